@@ -1,0 +1,210 @@
+"""ctypes binding of libmoe.so (include/moe.h), same entry-point names.
+
+Argument marshalling only: torch tensors become device pointers, the
+current CUDA stream becomes the stream argument, and a non-OK status raises
+MoeError.  All computation happens in the library's CUDA kernels.  There is
+no fallback: if libmoe.so is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_CUDA = 3
+MOE_ERR_TIMEOUT = 4
+MOE_ERR_INDEX = 5
+
+MOE_BF16 = 0
+MOE_F32 = 1
+
+MOE_SCORE_SOFTMAX_TOPK = 0
+MOE_SCORE_SOFTMAX_FULL = 1
+MOE_SCORE_SIGMOID_BIAS = 2
+
+SCORE_CODES = {"softmax_topk": MOE_SCORE_SOFTMAX_TOPK,
+               "softmax_full": MOE_SCORE_SOFTMAX_FULL,
+               "sigmoid_bias": MOE_SCORE_SIGMOID_BIAS}
+
+EXPORTED = ["moe_route_workspace_size", "moe_route",
+            "moe_dispatch_layout_workspace_size", "moe_dispatch_layout",
+            "moe_permute", "moe_grouped_ffn_workspace_size",
+            "moe_grouped_ffn", "moe_combine", "moe_selftest_bounded_wait",
+            "moe_selftest_sigmoid_key",
+            "moe_status_str", "moe_abi_version"]
+ABI_VERSION = 1
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: {status_str(code)} ({code})")
+
+
+class RouteCfg(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("score", ctypes.c_int32),
+                ("n_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
+                ("group_score_topk", ctypes.c_int32)]
+
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_sz = ctypes.c_size_t
+_u64 = ctypes.c_uint64
+
+_SIGS = {
+    "moe_route_workspace_size": (_sz, [ctypes.POINTER(RouteCfg)]),
+    "moe_route": (_i32, [ctypes.POINTER(RouteCfg), _vp, _vp, _vp, _vp, _vp,
+                         _vp, _vp, _vp, _sz, _vp, _vp]),
+    "moe_dispatch_layout_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "moe_dispatch_layout": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _vp,
+                                   _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                   _sz, _vp, _vp]),
+    "moe_permute": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "moe_grouped_ffn_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "moe_grouped_ffn": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
+                               _vp, _vp, _vp, _sz, _vp, _vp]),
+    "moe_combine": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "moe_selftest_bounded_wait": (_i32, [_vp, _u64, _vp]),
+    "moe_selftest_sigmoid_key": (_i32, [_vp, _vp, _i32, _vp]),
+    "moe_status_str": (ctypes.c_char_p, [_i32]),
+    "moe_abi_version": (_i32, []),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libmoe.so (raises OSError if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise OSError(
+                f"{path} not found: build it with "
+                "`python -m combine_router_gemm_top_b300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if lib.moe_abi_version() != ABI_VERSION:
+            raise OSError("libmoe.so ABI version mismatch; rebuild it")
+        _lib = lib
+    return _lib
+
+
+def status_str(code: int) -> str:
+    return load().moe_status_str(int(code)).decode()
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _check(rc, where):
+    if rc != MOE_OK:
+        raise MoeError(rc, where)
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return MOE_BF16
+    if dt == torch.float32:
+        return MOE_F32
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def route_cfg(T, D, E, k, dtype, score, n_groups=1, topk_groups=1,
+              group_score_topk=0) -> RouteCfg:
+    if isinstance(dtype, torch.dtype):
+        dtype = dtype_code(dtype)
+    if isinstance(score, str):
+        score = SCORE_CODES[score]
+    return RouteCfg(T, D, E, k, dtype, score, n_groups, topk_groups,
+                    group_score_topk)
+
+
+def moe_route_workspace_size(cfg: RouteCfg) -> int:
+    return load().moe_route_workspace_size(ctypes.byref(cfg))
+
+
+def moe_route(cfg, x, w_r, logit_offset, sel_bias, topk_idx, topk_gate,
+              logits_out, workspace, status, stream=None):
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().moe_route(ctypes.byref(cfg), _p(x), _p(w_r),
+                            _p(logit_offset), _p(sel_bias), _p(topk_idx),
+                            _p(topk_gate), _p(logits_out), _p(workspace),
+                            nbytes, _p(status), _stream(stream)),
+           "moe_route")
+
+
+def moe_dispatch_layout_workspace_size(T, k, E) -> int:
+    return load().moe_dispatch_layout_workspace_size(T, k, E)
+
+
+def moe_dispatch_layout(T, k, E, R, capacity, topk_idx, expert_counts,
+                        expert_offsets, dst_row, src_pair, n_kept, n_dropped,
+                        rank_send_counts, rank_send_displs, workspace, status,
+                        stream=None):
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().moe_dispatch_layout(
+        T, k, E, R, capacity, _p(topk_idx), _p(expert_counts),
+        _p(expert_offsets), _p(dst_row), _p(src_pair), _p(n_kept),
+        _p(n_dropped), _p(rank_send_counts), _p(rank_send_displs),
+        _p(workspace), nbytes, _p(status), _stream(stream)),
+        "moe_dispatch_layout")
+
+
+def moe_permute(T, k, D, dtype, x, dst_row, xp, stream=None):
+    _check(load().moe_permute(T, k, D, dtype, _p(x), _p(dst_row), _p(xp),
+                              _stream(stream)), "moe_permute")
+
+
+def moe_grouped_ffn_workspace_size(E, D, F, max_rows, dtype) -> int:
+    return load().moe_grouped_ffn_workspace_size(E, D, F, max_rows, dtype)
+
+
+def moe_grouped_ffn(E, D, F, max_rows, dtype, xp, expert_offsets, w13, w2,
+                    yp, workspace, status, stream=None):
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().moe_grouped_ffn(E, D, F, max_rows, dtype, _p(xp),
+                                  _p(expert_offsets), _p(w13), _p(w2),
+                                  _p(yp), _p(workspace), nbytes, _p(status),
+                                  _stream(stream)), "moe_grouped_ffn")
+
+
+def moe_combine(T, k, D, dtype, yp, dst_row, topk_gate, y, stream=None):
+    _check(load().moe_combine(T, k, D, dtype, _p(yp), _p(dst_row),
+                              _p(topk_gate), _p(y), _stream(stream)),
+           "moe_combine")
+
+
+def moe_selftest_bounded_wait(status, limit_ns, stream=None):
+    _check(load().moe_selftest_bounded_wait(_p(status), int(limit_ns),
+                                            _stream(stream)),
+           "moe_selftest_bounded_wait")
+
+
+def moe_selftest_sigmoid_key(l, out, stream=None):
+    _check(load().moe_selftest_sigmoid_key(_p(l), _p(out), l.numel(),
+                                           _stream(stream)),
+           "moe_selftest_sigmoid_key")

@@ -1,0 +1,179 @@
+// moe_grouped_ffn: per-expert SwiGLU over ragged, expert-contiguous row
+// segments ("Expert Parallelism in LLMs", The Execution Pipeline, step 4
+// "Local Expert Computation": the tokens of one expert packed into one
+// GEMM; Modern Dropless Dynamic Dispatch: ragged grouped GEMM on exact
+// per-expert counts, no padding).
+//
+// bf16: two persistent tcgen05 launches over a device-side tile list built
+// from expert_offsets (no host synchronisation):
+//   up    H[r, n:n+128]  = SiLU(Xp W1^T) * (Xp W3^T) for a 128-row block of
+//         one expert; B tile = 128 W1 rows stacked on the matching 128 W3
+//         rows, so gate and up land in one 128 x 256 TMEM accumulator and
+//         the GLU is applied in the epilogue (H rounded to bf16).
+//   down  Yp[r, n:n+256] = H W2^T.
+// Tiles run m-block-fastest inside (expert, n-block), so the CTAs working
+// at the same time share the weight tile through L2.
+// fp32: plain FMA kernels, one thread per output element.
+#include "common.cuh"
+#include "internal.h"
+#include "umma_gemm.cuh"
+
+namespace moe {
+
+// ----------------------------------------------------------- fp32 path
+__device__ __forceinline__ int find_expert(const int32_t* off, int E, int row) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(off + mid) <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void ffn_up_f32_kernel(int E, int D, int F, int max_rows,
+                                  const float* __restrict__ xp,
+                                  const int32_t* __restrict__ off,
+                                  const float* __restrict__ w13,
+                                  float* __restrict__ h) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int n_rows = min(__ldg(off + E), max_rows);
+  if (i >= static_cast<int64_t>(n_rows) * F) return;
+  const int row = static_cast<int>(i / F);
+  const int f = static_cast<int>(i - static_cast<int64_t>(row) * F);
+  const int e = find_expert(off, E, row);
+  const float* x = xp + static_cast<int64_t>(row) * D;
+  const float* w1 = w13 + (static_cast<int64_t>(e) * 2 * F + f) * D;
+  const float* w3 = w1 + static_cast<int64_t>(F) * D;
+  float g = 0.0f, u = 0.0f;
+  for (int d = 0; d < D; ++d) {
+    g = fmaf(x[d], w1[d], g);
+    u = fmaf(x[d], w3[d], u);
+  }
+  h[i] = g / (1.0f + expf(-g)) * u;
+}
+
+__global__ void ffn_down_f32_kernel(int E, int D, int F, int max_rows,
+                                    const float* __restrict__ h,
+                                    const int32_t* __restrict__ off,
+                                    const float* __restrict__ w2,
+                                    float* __restrict__ yp) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int n_rows = min(__ldg(off + E), max_rows);
+  if (i >= static_cast<int64_t>(n_rows) * D) return;
+  const int row = static_cast<int>(i / D);
+  const int d = static_cast<int>(i - static_cast<int64_t>(row) * D);
+  const int e = find_expert(off, E, row);
+  const float* hr = h + static_cast<int64_t>(row) * F;
+  const float* w = w2 + (static_cast<int64_t>(e) * D + d) * F;
+  float acc = 0.0f;
+  for (int f = 0; f < F; ++f) acc = fmaf(hr[f], w[f], acc);
+  yp[i] = acc;
+}
+
+// ----------------------------------------------------------- host
+size_t ffn_ws_bytes(int E, int D, int F, int max_rows, int dtype) {
+  (void)E;
+  (void)D;
+  return static_cast<size_t>(max_rows) * F * dtype_bytes(dtype);
+}
+
+template <int MODE>
+static moe_status launch_umma(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const GemmArgs& g, cudaStream_t stream,
+                              int num_sms) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(umma_gemm_kernel<MODE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             227 * 1024) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  const size_t smem = umma_gemm_smem_bytes(g.BN, g.stages);
+  umma_gemm_kernel<MODE><<<num_sms, kGemmThreads, smem, stream>>>(tmA, tmB, g);
+  return launch_status();
+}
+
+moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
+                              const void* xp, const int32_t* offsets,
+                              const void* w13, const void* w2, void* yp,
+                              void* ws, int32_t* status, cudaStream_t stream,
+                              int num_sms) {
+  if (max_rows == 0) return MOE_OK;
+  if (dtype == MOE_F32) {
+    float* h = static_cast<float*>(ws);
+    const int64_t n1 = static_cast<int64_t>(max_rows) * F;
+    ffn_up_f32_kernel<<<static_cast<unsigned>(ceil_div(n1, 256)), 256, 0,
+                        stream>>>(E, D, F, max_rows,
+                                  static_cast<const float*>(xp), offsets,
+                                  static_cast<const float*>(w13), h);
+    const int64_t n2 = static_cast<int64_t>(max_rows) * D;
+    ffn_down_f32_kernel<<<static_cast<unsigned>(ceil_div(n2, 256)), 256, 0,
+                          stream>>>(E, D, F, max_rows, h, offsets,
+                                    static_cast<const float*>(w2),
+                                    static_cast<float*>(yp));
+    return launch_status();
+  }
+  void* h = ws;
+  CUtensorMap tm_xp, tm_w13, tm_h, tm_w2;
+  if (!make_tmap_bf16_2d(&tm_xp, xp, D, max_rows, kBM) ||
+      !make_tmap_bf16_2d(&tm_w13, w13, D, static_cast<int64_t>(E) * 2 * F, 128) ||
+      !make_tmap_bf16_2d(&tm_h, h, F, max_rows, kBM) ||
+      !make_tmap_bf16_2d(&tm_w2, w2, F, static_cast<int64_t>(E) * D, 256))
+    return MOE_ERR_CUDA;
+
+  GemmArgs up{};
+  up.M = max_rows;
+  up.k_blocks = D / kBK;
+  up.BN = 256;
+  up.stages = 4;
+  up.tmem_cols = 512;
+  up.groups = E;
+  up.n_tiles = F / 128;
+  up.F = F;
+  up.b_rows_per_group = 2 * F;
+  up.offsets = offsets;
+  up.out = h;
+  up.out_ld = F;
+  up.out_cols = F;
+  up.status = status;
+  up.wait_limit_ns = kWaitLimitNs;
+  moe_status s = launch_umma<kUp>(tm_xp, tm_w13, up, stream, num_sms);
+  if (s != MOE_OK) return s;
+
+  GemmArgs dn = up;
+  dn.k_blocks = F / kBK;
+  dn.n_tiles = static_cast<int>(ceil_div(D, 256));
+  dn.F = 0;
+  dn.b_rows_per_group = D;
+  dn.out = yp;
+  dn.out_ld = D;
+  dn.out_cols = D;
+  return launch_umma<kDown>(tm_h, tm_w2, dn, stream, num_sms);
+}
+
+// ----------------------------------------------------------- self-test
+// Waits on a barrier that nothing arrives on; the bounded wait must expire,
+// raise the abort flag and report MOE_ERR_TIMEOUT.
+__global__ void selftest_wait_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const bool ok = mbar_wait(&bar, 0, &abort_flag, limit_ns);
+    if (!ok && abort_flag) set_status(status, MOE_ERR_TIMEOUT);
+  }
+}
+
+moe_status launch_selftest_wait(int32_t* status, uint64_t limit_ns,
+                                cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return launch_status();
+}
+
+}  // namespace moe

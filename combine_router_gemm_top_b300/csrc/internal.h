@@ -1,0 +1,80 @@
+// Internal host-side interfaces between the C-ABI layer (api.cu) and the
+// kernel files.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Upper bound on any single wait inside a kernel (a stalled pipeline
+// reports MOE_ERR_TIMEOUT instead of hanging the GPU).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box of 64
+// columns (128 bytes, 128-byte swizzle) by box_rows rows; out-of-bounds
+// elements read as zero.
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, int64_t cols,
+                       int64_t rows, int box_rows);
+
+struct RoutePlan {
+  int Npad;          // E rounded up to 16 (MMA N)
+  int k_blocks;      // ceil(D / 64)
+  int splits;        // split-K factor of the router GEMM
+  int kb_per_split;
+  size_t ws_bytes;   // partial logits [splits][T][E] fp32
+};
+RoutePlan plan_route(const moe_route_cfg& c, int num_sms);
+
+struct RouteSelectArgs {
+  int T, E, k, score, n_groups, topk_groups, group_score_topk, splits;
+  const float* partial;
+  const float* logit_offset;
+  const float* sel_bias;
+  int32_t* topk_idx;
+  float* topk_gate;
+  float* logits_out;
+};
+
+moe_status launch_route(const moe_route_cfg& c, const void* x, const void* w_r,
+                        const float* logit_offset, const float* sel_bias,
+                        int32_t* topk_idx, float* topk_gate, float* logits_out,
+                        void* ws, int32_t* status, cudaStream_t stream,
+                        int num_sms);
+
+constexpr int kLayoutChunk = 2048;   // pairs per layout block
+constexpr int kLayoutMaxE = 1024;
+constexpr int kMaxGroupsApi = 1024;   // experts the grouped tcgen05 scheduler handles
+size_t layout_ws_bytes(int64_t P, int E);
+moe_status launch_layout(int T, int k, int E, int R, int capacity,
+                         const int32_t* topk_idx, int32_t* expert_counts,
+                         int32_t* expert_offsets, int32_t* dst_row,
+                         int32_t* src_pair, int32_t* n_kept,
+                         int32_t* n_dropped, int32_t* rank_send_counts,
+                         int32_t* rank_send_displs, void* ws, int32_t* status,
+                         cudaStream_t stream);
+
+moe_status launch_permute(int T, int k, int D, int dtype, const void* x,
+                          const int32_t* dst_row, void* xp,
+                          cudaStream_t stream, int num_sms);
+moe_status launch_combine(int T, int k, int D, int dtype, const void* yp,
+                          const int32_t* dst_row, const float* gate, void* y,
+                          cudaStream_t stream, int num_sms);
+
+size_t ffn_ws_bytes(int E, int D, int F, int max_rows, int dtype);
+moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
+                              const void* xp, const int32_t* offsets,
+                              const void* w13, const void* w2, void* yp,
+                              void* ws, int32_t* status, cudaStream_t stream,
+                              int num_sms);
+
+moe_status launch_sigmoid_key(const float* l, float* out, int n,
+                              cudaStream_t stream);
+moe_status launch_selftest_wait(int32_t* status, uint64_t limit_ns,
+                                cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,433 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a:
+//   C[128 x BN tile] = A[rows, K] . B[cols, K]^T,  bf16 in, fp32 in TMEM.
+//
+// One CTA per SM, 6 warps:
+//   warp 0      TMA producer (one elected lane): A and B tiles into a ring of
+//               shared-memory stages (128-byte swizzle), completion counted
+//               on per-stage "full" mbarriers.
+//   warp 1      MMA issuer (one lane) and TMEM owner: 4 x tcgen05.mma
+//               (128 x BN x 16) per 64-wide K block; tcgen05.commit frees the
+//               stage ("empty" barrier) and, after the last K block,
+//               publishes the accumulator ("tfull").  Two accumulators
+//               alternate so the epilogue of tile i overlaps the MMAs of
+//               tile i+1.
+//   warps 2-5   epilogue: tcgen05.ld of their 32 TMEM lanes (one tile row
+//               per thread), the mode's math, 16-byte stores, then "tempty".
+//
+// Three modes share the pipeline and differ in tile scheduling, the B
+// operand rows and the epilogue:
+//   kRoute  router logits, split-K: tile = (m block, K split); writes fp32
+//           partial logits [split][T][E].
+//   kUp     grouped SwiGLU up-projection: tile = (expert, n block, m block)
+//           over ragged expert segments; B = 128 gate rows of W1 stacked on
+//           the matching 128 up rows of W3 (BN = 256), epilogue
+//           H = SiLU(gate) * up rounded to bf16.
+//   kDown   grouped down-projection: B = 256 rows of W2, epilogue rounds to
+//           bf16.
+// Every wait is time-bounded (see mbar_wait); on expiry the CTA stops
+// issuing, drains its own copies and MMAs, frees TMEM, and reports
+// MOE_ERR_TIMEOUT.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+enum GemmMode { kRoute = 0, kUp = 1, kDown = 2 };
+
+constexpr int kBM = 128;          // tile rows (TMEM lanes)
+constexpr int kBK = 64;           // K elements per stage (one 128-byte row)
+constexpr int kUmmaK = 16;        // K per tcgen05.mma for 16-bit inputs
+constexpr int kMaxStages = 8;
+constexpr int kGemmThreads = 192;
+constexpr int kMaxGroups = 1024;  // experts the grouped scheduler handles
+constexpr uint32_t kATileBytes = kBM * kBK * 2;
+
+struct GemmArgs {
+  int32_t M;                // route: T ; grouped: rows allocated (max_rows)
+  int32_t k_blocks;         // K / 64 (rounded up)
+  int32_t BN;               // N tile (route: E rounded up to 16; else 256)
+  int32_t stages;           // shared-memory ring depth
+  int32_t tmem_cols;        // power of two >= 2 * BN
+  // route
+  int32_t splits, kb_per_split, E;
+  // grouped
+  int32_t groups;           // experts
+  int32_t n_tiles;          // N blocks per expert
+  int32_t F;                // up: gate/up row split inside W13
+  int32_t b_rows_per_group; // up: 2F ; down: D
+  const int32_t* offsets;   // [groups + 1] expert row offsets
+  // output
+  void* out;
+  int32_t out_ld;           // elements per output row
+  int32_t out_cols;         // valid output columns
+  int32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+struct TileInfo {
+  int32_t a_row;      // first A row (TMA coordinate)
+  int32_t rows;       // valid rows in the tile (1..128)
+  int32_t b_row;      // first B row
+  int32_t b_row2;     // second B half (up mode)
+  int32_t out_col;    // first output column
+  int32_t kb_begin, kb_end;
+  int32_t split;      // route
+};
+
+struct GemmShared {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t abort;
+  int32_t total_tiles;
+  int32_t prefix[kMaxGroups + 1];   // grouped: first tile of each expert
+};
+
+template <int MODE>
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a,
+                                                const GemmShared& sh, int t) {
+  TileInfo ti;
+  if (MODE == kRoute) {
+    const int m_tiles = (a.M + kBM - 1) / kBM;
+    const int m = t % m_tiles;
+    ti.split = t / m_tiles;
+    ti.a_row = m * kBM;
+    ti.rows = min(kBM, a.M - ti.a_row);
+    ti.b_row = 0;
+    ti.b_row2 = 0;
+    ti.out_col = 0;
+    ti.kb_begin = ti.split * a.kb_per_split;
+    ti.kb_end = min(a.k_blocks, ti.kb_begin + a.kb_per_split);
+    return ti;
+  }
+  // binary search: the expert whose tile range holds t
+  int lo = 0, hi = a.groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sh.prefix[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int row0 = __ldg(a.offsets + e);
+  const int cnt = __ldg(a.offsets + e + 1) - row0;
+  const int m_tiles = (cnt + kBM - 1) / kBM;
+  const int local = t - sh.prefix[e];
+  const int n = local / m_tiles;
+  const int m = local - n * m_tiles;
+  ti.split = 0;
+  ti.a_row = row0 + m * kBM;
+  ti.rows = min(kBM, cnt - m * kBM);
+  ti.kb_begin = 0;
+  ti.kb_end = a.k_blocks;
+  if (MODE == kUp) {
+    ti.b_row = e * a.b_rows_per_group + n * 128;
+    ti.b_row2 = e * a.b_rows_per_group + a.F + n * 128;
+    ti.out_col = n * 128;
+  } else {
+    ti.b_row = e * a.b_rows_per_group + n * 256;
+    ti.b_row2 = 0;
+    ti.out_col = n * 256;
+  }
+  return ti;
+}
+
+__device__ __forceinline__ float silu_f32(float g) {
+  return g / (1.0f + __expf(-g));
+}
+
+// Epilogue of one tile for the thread owning tile row `r` (TMEM lane r).
+template <int MODE>
+__device__ __forceinline__ void epilogue_row(const GemmArgs& a,
+                                             const TileInfo& ti,
+                                             uint32_t tmem_row, int r) {
+  const int64_t grow = static_cast<int64_t>(ti.a_row) + r;
+  const bool valid = r < ti.rows && grow >= 0 && grow < a.M;
+  if (MODE == kRoute) {
+    // partial logits [split][T][E] fp32
+    float* out = reinterpret_cast<float*>(a.out) +
+                 (static_cast<int64_t>(ti.split) * a.M + grow) * a.E;
+    for (int c = 0; c < a.BN; c += 16) {
+      float v[16];
+      tmem_ld16(tmem_row + c, v);
+      if (valid) {
+        if ((a.E & 3) == 0 && c + 16 <= a.E) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4*>(out + c + i) =
+                make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (c + i < a.E) out[c + i] = v[i];
+        }
+      }
+    }
+  } else if (MODE == kUp) {
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) +
+                         grow * a.out_ld + ti.out_col;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      float g[32], u[32];
+      tmem_ld32(tmem_row + c, g);
+      tmem_ld32(tmem_row + 128 + c, u);
+      if (valid) {
+        float h[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) h[i] = silu_f32(g[i]) * u[i];
+#pragma unroll
+        for (int i = 0; i < 32; i += 8)
+          st_v4(out + c + i, Vec16<__nv_bfloat16>::from_f32(h + i));
+      }
+    }
+  } else {
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) +
+                         grow * a.out_ld + ti.out_col;
+#pragma unroll 1
+    for (int c = 0; c < 256; c += 32) {
+      float v[32];
+      tmem_ld32(tmem_row + c, v);
+      if (valid && ti.out_col + c < a.out_cols) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 8)
+          st_v4(out + c + i, Vec16<__nv_bfloat16>::from_f32(v + i));
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
+                                                uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    umma_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte-swizzled tiles
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* tiles = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  const uint32_t b_tile_bytes = static_cast<uint32_t>(a.BN) * kBK * 2;
+  uint8_t* a_tiles = tiles;
+  uint8_t* b_tiles = tiles + a.stages * kATileBytes;
+  GemmShared& sh = *reinterpret_cast<GemmShared*>(
+      b_tiles + static_cast<size_t>(a.stages) * b_tile_bytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = &sh.abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.tfull[i], 1);
+      mbar_init(&sh.tempty[i], 4);
+    }
+    mbar_init(&sh.drain, 1);
+    sh.abort = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  // tile prefix over experts (grouped modes)
+  if (MODE != kRoute) {
+    if (warp == 2) {
+      int run = 0;
+      for (int base = 0; base < a.groups; base += 32) {
+        const int e = base + lane;
+        int tiles_e = 0;
+        if (e < a.groups) {
+          const int cnt = __ldg(a.offsets + e + 1) - __ldg(a.offsets + e);
+          tiles_e = (max(cnt, 0) + kBM - 1) / kBM * a.n_tiles;
+        }
+        int incl = tiles_e;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += v;
+        }
+        if (e < a.groups) sh.prefix[e] = run + incl - tiles_e;
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) {
+        sh.prefix[a.groups] = run;
+        sh.total_tiles = run;
+      }
+    }
+  } else if (threadIdx.x == 64) {
+    sh.total_tiles = ((a.M + kBM - 1) / kBM) * a.splits;
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, a.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const int total = sh.total_tiles;
+  const uint32_t tmem_base = sh.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      const uint32_t tx = kATileBytes + b_tile_bytes;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile<MODE>(a, sh, t);
+        for (int kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
+          if (!mbar_wait(&sh.empty[stage], phase ^ 1, abort_flag,
+                         a.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sh.full[stage], tx);
+          uint8_t* sa = a_tiles + stage * kATileBytes;
+          uint8_t* sb = b_tiles + static_cast<size_t>(stage) * b_tile_bytes;
+          tma_load_2d(sa, &tmA, &sh.full[stage], kb * kBK, ti.a_row);
+          if (MODE == kUp) {
+            tma_load_2d(sb, &tmB, &sh.full[stage], kb * kBK, ti.b_row);
+            tma_load_2d(sb + 128 * 128, &tmB, &sh.full[stage], kb * kBK,
+                        ti.b_row2);
+          } else {
+            tma_load_2d(sb, &tmB, &sh.full[stage], kb * kBK, ti.b_row);
+          }
+          ++issued;
+          if (++stage == a.stages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // drain the copies still in flight before the CTA may exit
+        const int n = min(issued, a.stages);
+        int s = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < n; ++i) {
+          if (s == 0) {
+            s = a.stages - 1;
+            ph ^= 1;
+          } else {
+            --s;
+          }
+          mbar_wait_drain(&sh.full[s], ph, 50000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      const uint32_t idesc = umma_idesc_bf16(kBM, a.BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+        const TileInfo ti = decode_tile<MODE>(a, sh, t);
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait(&sh.tempty[acc], acc_phase ^ 1, abort_flag,
+                       a.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * a.BN;
+        for (int kb = ti.kb_begin; kb < ti.kb_end; ++kb) {
+          if (!mbar_wait(&sh.full[stage], phase, abort_flag,
+                         a.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(a_tiles + stage * kATileBytes);
+          const uint32_t sb =
+              smem_u32(b_tiles + static_cast<size_t>(stage) * b_tile_bytes);
+          const uint64_t adesc = umma_desc_sw128(sa);
+          const uint64_t bdesc = umma_desc_sw128(sb);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            // +32 bytes along K per step: +2 in the >>4 address field
+            umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+                      (kb > ti.kb_begin || k > 0) ? 1u : 0u);
+          }
+          umma_commit(&sh.empty[stage]);
+          if (++stage == a.stages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&sh.tfull[acc]);
+      }
+      if (!ok) {
+        umma_commit(&sh.drain);
+        mbar_wait_drain(&sh.drain, 0, 50000000ull);
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5
+    const int quarter = warp & 3;          // TMEM lanes 32*quarter ..
+    const int r = quarter * 32 + lane;     // tile row of this thread
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      const TileInfo ti = decode_tile<MODE>(a, sh, t);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      bool ok = true;
+      if (lane == 0)
+        ok = mbar_wait(&sh.tfull[acc], acc_phase, abort_flag, a.wait_limit_ns);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tmem_row =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+          acc * a.BN;
+      epilogue_row<MODE>(a, ti, tmem_row, r);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.tempty[acc]);
+    }
+  }
+
+  __syncwarp();   // reconverge the single-lane producer / MMA roles
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, a.tmem_cols);
+  }
+  if (threadIdx.x == 0 && sh.abort) set_status(a.status, MOE_ERR_TIMEOUT);
+}
+
+// Shared-memory bytes of one launch (tiles + control block + alignment slack).
+inline size_t umma_gemm_smem_bytes(int BN, int stages) {
+  return 1024 + static_cast<size_t>(stages) * (kATileBytes + BN * kBK * 2) +
+         sizeof(GemmShared);
+}
+
+}  // namespace moe

@@ -1,0 +1,144 @@
+"""Host-side MoE layer: owns the device buffers of one layer pass and calls
+the five C-ABI entry points in order on one stream.
+
+    route -> dispatch_layout -> permute -> grouped_ffn -> combine
+
+("Expert Parallelism in LLMs", The Execution Pipeline, steps 1, 2, 4 and 6;
+on one GPU the all-to-all steps 3 and 5 are the identity).  Buffers are
+sized for the worst case (T*k rows) so no step ever waits on the host for
+the dropless row count: expert offsets and kept counts stay on the device.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+from typing import Optional
+
+import torch
+
+from . import _lib as L
+
+
+def expert_capacity(capacity_factor, T, k, E) -> int:
+    """C_expert = ceil(CF * k * T / E) in exact rational arithmetic; 0 means
+    dropless ("Expert Parallelism in LLMs", Static Capacity Factors and Token
+    Dropping)."""
+    if capacity_factor is None:
+        return 0
+    return math.ceil(Fraction(str(capacity_factor)) * k * T / E)
+
+
+class MoELayer:
+    """One MoE layer forward pass on one GPU.
+
+    Weights are device tensors in the layer dtype (bf16 or fp32):
+      w_r [E, D], w13 [E, 2F, D] (gate rows then up rows), w2 [E, D, F];
+      w13 = w2 = None selects identity experts (Expert_i(h) = h).
+    """
+
+    def __init__(self, T, D, E, k, R, w_r, w13=None, w2=None, F=0,
+                 score="softmax_topk", sel_bias=None, logit_offset=None,
+                 capacity_factor=None, n_groups=1, topk_groups=1,
+                 group_score_topk=0, device=None, keep_logits=False):
+        L.load()
+        self.device = torch.device(device or w_r.device)
+        self.dtype = w_r.dtype
+        self.dcode = L.dtype_code(self.dtype)
+        self.T, self.D, self.E, self.k, self.R, self.F = T, D, E, k, R, F
+        self.identity = w13 is None
+        self.w_r, self.w13, self.w2 = w_r, w13, w2
+        self.sel_bias, self.logit_offset = sel_bias, logit_offset
+        self.capacity = expert_capacity(capacity_factor, T, k, E)
+        self.cfg = L.route_cfg(T, D, E, k, self.dcode, score, n_groups,
+                               topk_groups, group_score_topk)
+        P = T * k
+        dev = self.device
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.topk_idx = torch.empty((T, k), **i32)
+        self.topk_gate = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.logits = (torch.empty((T, E), dtype=torch.float32, device=dev)
+                       if keep_logits else None)
+        self.route_ws = self._bytes(L.moe_route_workspace_size(self.cfg))
+        self.layout_ws = self._bytes(
+            L.moe_dispatch_layout_workspace_size(T, k, E))
+        self.expert_counts = torch.empty(E, **i32)
+        self.expert_offsets = torch.empty(E + 1, **i32)
+        self.dst_row = torch.empty(P, **i32)
+        self.src_pair = torch.empty(P, **i32)
+        self.n_kept = torch.empty(1, **i32)
+        self.n_dropped = torch.empty(1, **i32)
+        self.rank_send_counts = torch.empty(R, **i32)
+        self.rank_send_displs = torch.empty(R, **i32)
+        self.xp = torch.empty((max(P, 1), D), dtype=self.dtype, device=dev)
+        if self.identity:
+            self.yp = self.xp
+            self.ffn_ws = None
+        else:
+            self.yp = torch.empty((max(P, 1), D), dtype=self.dtype,
+                                  device=dev)
+            self.ffn_ws = self._bytes(L.moe_grouped_ffn_workspace_size(
+                E, D, F, P, self.dcode))
+        self.y = torch.empty((T, D), dtype=self.dtype, device=dev)
+        self.status = torch.zeros(1, **i32)
+
+    def _bytes(self, n):
+        # 256-byte aligned scratch (torch's allocator aligns to >= 512 B)
+        return torch.empty(max(int(n), 16), dtype=torch.uint8,
+                           device=self.device)
+
+    # ---------------------------------------------------------- steps
+    def route(self, x, stream=None):
+        L.moe_route(self.cfg, x, self.w_r, self.logit_offset, self.sel_bias,
+                    self.topk_idx, self.topk_gate, self.logits,
+                    self.route_ws, self.status, stream)
+
+    def dispatch_layout(self, topk_idx=None, stream=None):
+        idx = self.topk_idx if topk_idx is None else topk_idx
+        L.moe_dispatch_layout(
+            self.T, self.k, self.E, self.R, self.capacity, idx,
+            self.expert_counts, self.expert_offsets, self.dst_row,
+            self.src_pair, self.n_kept, self.n_dropped, self.rank_send_counts,
+            self.rank_send_displs, self.layout_ws, self.status, stream)
+
+    def permute(self, x, stream=None):
+        L.moe_permute(self.T, self.k, self.D, self.dcode, x, self.dst_row,
+                      self.xp, stream)
+
+    def grouped_ffn(self, stream=None):
+        if self.identity:
+            return
+        L.moe_grouped_ffn(self.E, self.D, self.F, self.T * self.k, self.dcode,
+                          self.xp, self.expert_offsets, self.w13, self.w2,
+                          self.yp, self.ffn_ws, self.status, stream)
+
+    def combine(self, topk_gate=None, y=None, stream=None):
+        gate = self.topk_gate if topk_gate is None else topk_gate
+        out = self.y if y is None else y
+        L.moe_combine(self.T, self.k, self.D, self.dcode, self.yp,
+                      self.dst_row, gate, out, stream)
+        return out
+
+    # ---------------------------------------------------------- layer
+    def forward(self, x, topk_idx=None, topk_gate=None, y=None, stream=None):
+        """y = MoE(x) for x [T, D] on the device.  With topk_idx/topk_gate
+        given, routing is taken from them (pre-drawn routing) and moe_route
+        is skipped."""
+        if topk_idx is None:
+            self.route(x, stream)
+        self.dispatch_layout(topk_idx, stream)
+        self.permute(x, stream)
+        self.grouped_ffn(stream)
+        return self.combine(topk_gate, y, stream)
+
+    def forward_host(self, x_host, y_host, x_dev, stream=None):
+        """End-to-end pass from pinned host memory: copy x in, run the
+        layer, copy y out, all on one stream."""
+        s = stream or torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            x_dev.copy_(x_host, non_blocking=True)
+            self.forward(x_dev, stream=s)
+            y_host.copy_(self.y, non_blocking=True)
+        return y_host
+
+    def device_status(self) -> int:
+        return int(self.status.item())

@@ -1,0 +1,252 @@
+/*
+ * moe.h -- C ABI of libmoe.so, the forward pass of a mixture-of-experts
+ * layer on one B300 GPU (sm_103a):
+ *
+ *   y_t = sum over the top-k experts i of g_i(x_t) * Expert_i(x_t)
+ *   ("Expert Parallelism in LLMs: How All-to-All Token Dispatch, Capacity
+ *    Factors, and Parallel Folding Scale MoE Architectures", section
+ *    "The Distributed MoE Dilemma: Dense vs. Sparse Sharding", the MoE
+ *    layer equation)
+ *
+ * The five calls follow that page's section "The Execution Pipeline":
+ *   moe_route            step 1, router gating and top-k selection
+ *   moe_dispatch_layout  step 2, local permutation layout, plus the
+ *                        per-rank send counts of step 3's all-to-all-v
+ *   moe_permute          step 2, the physical reorder into the
+ *                        expert-contiguous buffer
+ *   moe_grouped_ffn      step 4, batched GEMM per local expert (SwiGLU)
+ *   moe_combine          step 6, un-permutation and weighted reduction
+ * On one GPU the dispatch and combine all-to-alls (steps 3 and 5) are the
+ * identity: the expert-contiguous buffer is the send buffer, split by
+ * rank_send_counts / rank_send_displs.
+ *
+ * Conventions shared by every call
+ *  - Pointers are DEVICE pointers unless marked "host".  The caller owns
+ *    every buffer, including workspaces; the library keeps no allocation
+ *    between calls and never allocates, synchronises or copies to the host.
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default
+ *    stream).  A return of MOE_OK means the work was enqueued.
+ *  - Errors the host can see (null pointer, bad size, misaligned pointer,
+ *    unsupported shape or dtype) return MOE_ERR_INVALID or
+ *    MOE_ERR_UNSUPPORTED and launch nothing.  A failed launch returns
+ *    MOE_ERR_CUDA.
+ *  - Errors only the device can see are written to the optional `status`
+ *    word (one int32 in device memory, 0 = OK): the first error code wins
+ *    (atomic compare-and-swap from 0).  The caller clears it and reads it
+ *    when it chooses.  Kernels never trap: out-of-range data is skipped and
+ *    reported, and every wait on another warp is bounded in time.
+ *  - Matrices are row-major.  "K-major" means the reduction dimension is
+ *    contiguous.  Rows of activations must start on 16-byte boundaries:
+ *    D * sizeof(element) must be a multiple of 16, and base pointers must be
+ *    16-byte aligned (256-byte for buffers read by the tensor-memory
+ *    accelerator, noted per call).
+ *  - Pair id p = t * k + j names slot j (0 = highest score) of token t.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = 1,     /* bad argument, detected on the host           */
+  MOE_ERR_UNSUPPORTED = 2, /* valid request outside what this build runs    */
+  MOE_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed          */
+  MOE_ERR_TIMEOUT = 4,     /* device: a bounded wait expired                */
+  MOE_ERR_INDEX = 5        /* device: an expert id outside [0, E)           */
+} moe_status;
+
+typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
+
+/* How router logits become selection keys and gates. */
+typedef enum {
+  /* key = logit; gate = softmax over the k selected logits,
+   * g_t = Softmax(TopK(W_g x_t, k)) ("Expert Parallelism in LLMs",
+   * The Execution Pipeline, step 1). */
+  MOE_SCORE_SOFTMAX_TOPK = 0,
+  /* key = logit; gate = softmax over all E experts, taken at the selected
+   * ones (the top-1 Switch-style gate). */
+  MOE_SCORE_SOFTMAX_FULL = 1,
+  /* s = sigmoid(logit) in fp32, key = s + sel_bias[e] (bias steers
+   * selection only); gate = s_j / sum of the selected s ("Expert
+   * Parallelism in LLMs", Modern Dropless Dynamic Dispatch: bias terms on
+   * routing scores for auxiliary-loss-free balance). */
+  MOE_SCORE_SIGMOID_BIAS = 2
+} moe_score;
+
+/* Router configuration.  Group-limited selection (n_groups > 1): experts
+ * form n_groups contiguous groups; a group's score is the fp32 sum of its
+ * group_score_topk largest keys (largest first); the topk_groups best
+ * groups stay eligible and the top-k is taken inside them ("Expert
+ * Parallelism and All-to-All", Three ways the system fights back: a token
+ * reaches at most a few nodes, chosen before the per-expert selection).
+ * Ties: equal keys go to the lower expert index, equal group scores to the
+ * lower group index.  n_groups = 1 disables grouping. */
+typedef struct {
+  int32_t T;                /* tokens                                   */
+  int32_t D;                /* hidden size                              */
+  int32_t E;                /* experts, 1..256                          */
+  int32_t k;                /* experts per token, 1..min(E, 32)         */
+  int32_t dtype;            /* moe_dtype of x and w_r                   */
+  int32_t score;            /* moe_score                                */
+  int32_t n_groups;         /* 1 = no grouping; must divide E           */
+  int32_t topk_groups;      /* groups kept, 1..n_groups                 */
+  int32_t group_score_topk; /* keys summed per group, 1..E/n_groups     */
+} moe_route_cfg;
+
+/* Bytes of scratch moe_route needs for `cfg` (partial fp32 logits of the
+ * split-K router GEMM).  Returns 0 for an invalid cfg. */
+MOE_API size_t moe_route_workspace_size(const moe_route_cfg* cfg);
+
+/* moe_route -- router GEMM, score, top-k and gates
+ * ("Expert Parallelism in LLMs", The Execution Pipeline, step 1 "Router
+ *  Gating and Softmax Selection"; "All-to-All Communication", phase 1
+ *  "Routing decision").
+ *   cfg           host pointer
+ *   x             [T, D] dtype, row-major, 256-byte aligned
+ *   w_r           [E, D] dtype, row-major (K-major), 256-byte aligned
+ *   logit_offset  [E] fp32 or NULL: added to every token's logits in fp32
+ *                 before scoring (it moves both selection and gates)
+ *   sel_bias      [E] fp32 or NULL: selection bias, sigmoid mode only
+ *   topk_idx      [T, k] int32 out: expert ids, slot 0 = best key
+ *   topk_gate     [T, k] fp32 out
+ *   logits_out    [T, E] fp32 out or NULL: the exact logits (after the
+ *                 offset) that selection used
+ *   workspace     >= moe_route_workspace_size(cfg) bytes, 16-byte aligned
+ * logits = fp32(x . w_r^T) accumulated in fp32 (bf16 inputs on the tensor
+ * cores for MOE_BF16; fp32 FMA for MOE_F32). */
+MOE_API moe_status moe_route(const moe_route_cfg* cfg, const void* x, const void* w_r,
+                     const float* logit_offset, const float* sel_bias,
+                     int32_t* topk_idx, float* topk_gate, float* logits_out,
+                     void* workspace, size_t workspace_bytes,
+                     int32_t* status, moe_stream_t stream);
+
+/* Bytes of scratch moe_dispatch_layout needs (per-chunk expert
+ * histograms).  Returns 0 for invalid sizes. */
+MOE_API size_t moe_dispatch_layout_workspace_size(int32_t T, int32_t k, int32_t E);
+
+/* moe_dispatch_layout -- binning of the T*k (token, expert) pairs into an
+ * expert-contiguous buffer ("Expert Parallelism in LLMs", The Execution
+ * Pipeline, step 2 "Local Token Permutation"; "All-to-All Communication",
+ * the expert_parallel_dispatch listing: destination = expert /
+ * experts_per_device, bincount of destinations as the send counts), with
+ * the capacity clamp C = ceil(CF * k * T / E) ("Expert Parallelism in
+ * LLMs", Static Capacity Factors and Token Dropping).
+ *   R             virtual expert-parallel ranks; must divide E; rank r owns
+ *                 experts [r*E/R, (r+1)*E/R)
+ *   capacity      rows per expert; <= 0 means dropless
+ *   topk_idx      [T*k] int32 in
+ *   expert_counts [E] out: kept pairs per expert = min(routed, capacity)
+ *   expert_offsets[E+1] out: exclusive scan of expert_counts
+ *   dst_row       [T*k] out: buffer row of pair p, -1 if dropped
+ *   src_pair      [T*k] out: pair id held by buffer row r, r < n_kept
+ *                 (entries past n_kept are left unwritten)
+ *   n_kept, n_dropped   [1] out each
+ *   rank_send_counts, rank_send_displs  [R] out: rows bound for each rank
+ *                 and where they start (the all-to-all-v split arguments)
+ *   workspace     >= moe_dispatch_layout_workspace_size(T, k, E) bytes
+ * Pairs are visited in pair-id order: within an expert, rows ascend with p,
+ * and a pair is kept iff fewer than `capacity` earlier pairs chose the same
+ * expert.  Ids outside [0, E) are dropped and raise MOE_ERR_INDEX in
+ * `status`.  Integer results are deterministic. */
+MOE_API moe_status moe_dispatch_layout(int32_t T, int32_t k, int32_t E, int32_t R,
+                               int32_t capacity, const int32_t* topk_idx,
+                               int32_t* expert_counts, int32_t* expert_offsets,
+                               int32_t* dst_row, int32_t* src_pair,
+                               int32_t* n_kept, int32_t* n_dropped,
+                               int32_t* rank_send_counts,
+                               int32_t* rank_send_displs,
+                               void* workspace, size_t workspace_bytes,
+                               int32_t* status, moe_stream_t stream);
+
+/* moe_permute -- xp[dst_row[t*k + j]] = x[t] for every kept pair
+ * ("Expert Parallelism in LLMs", The Execution Pipeline, step 2: tokens
+ * physically reordered into contiguous per-destination buffers).  Each
+ * token row is read once and written to each of its kept destinations.
+ *   x    [T, D] dtype in;  xp [>= n_kept, D] dtype out (rows not named by
+ *        dst_row are left unwritten).  16-byte aligned. */
+MOE_API moe_status moe_permute(int32_t T, int32_t k, int32_t D, int32_t dtype,
+                       const void* x, const int32_t* dst_row, void* xp,
+                       moe_stream_t stream);
+
+/* Bytes of scratch moe_grouped_ffn needs: the SwiGLU hidden activations
+ * H [max_rows, F] in the compute dtype. */
+MOE_API size_t moe_grouped_ffn_workspace_size(int32_t E, int32_t D, int32_t F,
+                                      int32_t max_rows, int32_t dtype);
+
+/* moe_grouped_ffn -- per-expert SwiGLU over ragged expert segments
+ * ("Expert Parallelism in LLMs", The Execution Pipeline, step 4 "Local
+ *  Expert Computation": the rows of one expert packed into one GEMM;
+ *  Modern Dropless Dynamic Dispatch: ragged grouped GEMM over exact
+ *  per-expert counts).  For every expert e and row r in
+ *  [expert_offsets[e], expert_offsets[e+1]):
+ *     H[r]  = SiLU(xp[r] . W1_e^T) * (xp[r] . W3_e^T)   (rounded to dtype)
+ *     yp[r] = H[r] . W2_e^T
+ *   xp      [max_rows, D] dtype, 256-byte aligned
+ *   w13     [E, 2F, D] dtype: rows 0..F-1 of each expert are W1 (gate),
+ *           rows F..2F-1 are W3 (up); K-major; 256-byte aligned
+ *   w2      [E, D, F] dtype, K-major; 256-byte aligned
+ *   yp      [max_rows, D] dtype out; rows >= expert_offsets[E] untouched
+ *   max_rows  rows allocated in xp / yp (>= expert_offsets[E]; T*k works)
+ * Expert offsets are read on the device: no host synchronisation.
+ * MOE_BF16 runs on the tcgen05 tensor cores with fp32 accumulation and
+ * needs D % 64 == 0 and F % 128 == 0 (else MOE_ERR_UNSUPPORTED);
+ * MOE_F32 runs fp32 FMA. */
+MOE_API moe_status moe_grouped_ffn(int32_t E, int32_t D, int32_t F, int32_t max_rows,
+                           int32_t dtype, const void* xp,
+                           const int32_t* expert_offsets, const void* w13,
+                           const void* w2, void* yp, void* workspace,
+                           size_t workspace_bytes, int32_t* status,
+                           moe_stream_t stream);
+
+/* moe_combine -- y[t] = sum over kept slots j of
+ * topk_gate[t, j] * yp[dst_row[t*k + j]], accumulated in fp32 in slot
+ * order, rounded once to dtype ("Expert Parallelism in LLMs", The Execution
+ * Pipeline, step 6 "Unpermutation and Weighted Reduction"; dropped pairs
+ * contribute nothing, "Static Capacity Factors and Token Dropping").  The
+ * residual connection is not added.  A token with no kept pair gets zeros.
+ *   yp [>= n_kept, D] dtype; y [T, D] dtype out; 16-byte aligned. */
+MOE_API moe_status moe_combine(int32_t T, int32_t k, int32_t D, int32_t dtype,
+                       const void* yp, const int32_t* dst_row,
+                       const float* topk_gate, void* y, moe_stream_t stream);
+
+/* Test hook for the bounded-wait machinery: launches one CTA that waits on
+ * a shared-memory barrier nothing arrives on, gives up after `limit_ns`
+ * nanoseconds, writes MOE_ERR_TIMEOUT into `status` and returns. */
+MOE_API moe_status moe_selftest_bounded_wait(int32_t* status, uint64_t limit_ns,
+                                     moe_stream_t stream);
+
+/* Test hook for the selection key of MOE_SCORE_SIGMOID_BIAS: out[i] = the
+ * fp32 sigmoid moe_route evaluates for logit l[i] (n values, device
+ * pointers).  Selection is an integer decision taken on these fp32 values,
+ * so a checker must reproduce them bit for bit. */
+MOE_API moe_status moe_selftest_sigmoid_key(const float* l, float* out,
+                                            int32_t n, moe_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char* moe_status_str(int32_t status);
+
+/* ABI version of this header (incremented on any signature change). */
+MOE_API int32_t moe_abi_version(void);
+
+#define MOE_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,139 @@
+"""CPU checks of the C ABI: libmoe.so builds and loads, exports every
+function include/moe.h declares, and rejects bad arguments on the host
+(MOE_ERR_INVALID / MOE_ERR_UNSUPPORTED) before launching anything.  No call
+here reaches a kernel, so these run without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from combine_router_gemm_top_b300 import _lib as L
+from combine_router_gemm_top_b300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build(verbose=False)
+    return L.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(",
+                                 text)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ("moe_route", "moe_dispatch_layout", "moe_permute",
+              "moe_grouped_ffn", "moe_combine"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert sorted(L.EXPORTED) == names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.moe_abi_version() == L.ABI_VERSION
+
+
+def test_status_strings(lib):
+    assert L.status_str(0) == "MOE_OK"
+    assert L.status_str(4) == "MOE_ERR_TIMEOUT"
+    assert L.status_str(99) == "MOE_ERR_UNKNOWN"
+
+
+FAKE = 1 << 20   # a non-null, 256-byte aligned address that is never touched
+
+
+def test_route_rejects_bad_configs(lib):
+    good = L.route_cfg(128, 256, 8, 2, L.MOE_BF16, L.MOE_SCORE_SOFTMAX_TOPK)
+    assert L.moe_route_workspace_size(good) > 0
+    bad = [L.route_cfg(128, 256, 8, 9, L.MOE_BF16, 0),       # k > E
+           L.route_cfg(128, 256, 300, 2, L.MOE_BF16, 0),     # E > 256
+           L.route_cfg(128, 250, 8, 2, L.MOE_BF16, 0),       # row not 16 B
+           L.route_cfg(128, 256, 8, 2, 7, 0),                # dtype
+           L.route_cfg(128, 256, 8, 2, L.MOE_BF16, 5),       # score
+           L.route_cfg(128, 256, 12, 2, L.MOE_BF16, 2, 5, 1, 1),   # groups
+           L.route_cfg(128, 256, 16, 8, L.MOE_BF16, 2, 4, 1, 2)]   # k > kept
+    for cfg in bad:
+        assert L.moe_route_workspace_size(cfg) == 0
+        rc = lib.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE,
+                           FAKE, None, FAKE, 1 << 30, None, None)
+        assert rc == L.MOE_ERR_INVALID
+    # null pointers and misalignment
+    rc = lib.moe_route(ctypes.byref(good), None, FAKE, None, None, FAKE, FAKE,
+                       None, FAKE, 1 << 30, None, None)
+    assert rc == L.MOE_ERR_INVALID
+    rc = lib.moe_route(ctypes.byref(good), FAKE + 16, FAKE, None, None, FAKE,
+                       FAKE, None, FAKE, 1 << 30, None, None)
+    assert rc == L.MOE_ERR_INVALID
+    # workspace too small
+    rc = lib.moe_route(ctypes.byref(good), FAKE, FAKE, None, None, FAKE, FAKE,
+                       None, FAKE, 4, None, None)
+    assert rc == L.MOE_ERR_INVALID
+
+
+def test_layout_rejects_bad_sizes(lib):
+    assert lib.moe_dispatch_layout_workspace_size(10, 2, 8) > 0
+    assert lib.moe_dispatch_layout_workspace_size(10, 33, 64) == 0
+    args = [FAKE] * 9 + [FAKE, 1 << 30, None, None]
+    assert lib.moe_dispatch_layout(10, 2, 8, 3, 0, *args) == L.MOE_ERR_INVALID
+    assert lib.moe_dispatch_layout(10, 2, 8, 0, 0, *args) == L.MOE_ERR_INVALID
+    assert lib.moe_dispatch_layout(10, 2, 2048, 8, 0, *args) == \
+        L.MOE_ERR_INVALID
+    assert lib.moe_dispatch_layout(1 << 30, 4, 8, 8, 0, *args) == \
+        L.MOE_ERR_INVALID                              # T*k overflows int32
+    small = [FAKE] * 9 + [FAKE, 4, None, None]
+    assert lib.moe_dispatch_layout(10, 2, 8, 4, 0, *small) == \
+        L.MOE_ERR_INVALID                              # workspace too small
+    nul = [FAKE] * 9 + [None, 1 << 30, None, None]
+    assert lib.moe_dispatch_layout(10, 2, 8, 4, 0, *nul) == L.MOE_ERR_INVALID
+
+
+def test_permute_combine_reject(lib):
+    assert lib.moe_permute(10, 2, 12, L.MOE_BF16, FAKE, FAKE, FAKE, None) == \
+        L.MOE_ERR_INVALID                              # 24-byte rows
+    assert lib.moe_permute(10, 2, 16, L.MOE_BF16, None, FAKE, FAKE, None) == \
+        L.MOE_ERR_INVALID
+    assert lib.moe_permute(10, 2, 16, L.MOE_BF16, FAKE + 8, FAKE, FAKE,
+                           None) == L.MOE_ERR_INVALID
+    assert lib.moe_combine(10, 40, 16, L.MOE_BF16, FAKE, FAKE, FAKE, FAKE,
+                           None) == L.MOE_ERR_INVALID   # k > 32
+    assert lib.moe_combine(10, 2, 16, 3, FAKE, FAKE, FAKE, FAKE, None) == \
+        L.MOE_ERR_INVALID
+    # nothing to do is not an error
+    assert lib.moe_permute(0, 2, 16, L.MOE_BF16, None, None, None, None) == \
+        L.MOE_OK
+
+
+def test_grouped_ffn_reject(lib):
+    ok_ws = 1 << 40
+    assert lib.moe_grouped_ffn(8, 100, 256, 64, L.MOE_BF16, FAKE, FAKE, FAKE,
+                               FAKE, FAKE, FAKE, ok_ws, None, None) == \
+        L.MOE_ERR_UNSUPPORTED                          # D % 64
+    assert lib.moe_grouped_ffn(8, 128, 200, 64, L.MOE_BF16, FAKE, FAKE, FAKE,
+                               FAKE, FAKE, FAKE, ok_ws, None, None) == \
+        L.MOE_ERR_UNSUPPORTED                          # F % 128
+    assert lib.moe_grouped_ffn(8, 128, 256, 64, L.MOE_BF16, FAKE + 16, FAKE,
+                               FAKE, FAKE, FAKE, FAKE, ok_ws, None, None) == \
+        L.MOE_ERR_INVALID                              # TMA base alignment
+    assert lib.moe_grouped_ffn(8, 128, 256, 64, L.MOE_BF16, FAKE, FAKE, FAKE,
+                               FAKE, FAKE, FAKE, 16, None, None) == \
+        L.MOE_ERR_INVALID                              # workspace too small
+    assert lib.moe_grouped_ffn(8, 128, 256, 64, L.MOE_BF16, FAKE, None, FAKE,
+                               FAKE, FAKE, FAKE, ok_ws, None, None) == \
+        L.MOE_ERR_INVALID
+    assert lib.moe_grouped_ffn_workspace_size(8, 128, 256, 64, L.MOE_BF16) == \
+        64 * 256 * 2
+
+
+def test_selftests_reject_null(lib):
+    assert lib.moe_selftest_bounded_wait(None, 10, None) == L.MOE_ERR_INVALID
+    assert lib.moe_selftest_sigmoid_key(None, None, 5, None) == \
+        L.MOE_ERR_INVALID

@@ -156,7 +156,7 @@ def test_group_limited_brute_force():
         idx, _ = O.route_from_logits(logits, k, O.SIGMOID_BIAS, bias,
                                      n_groups=G, topk_groups=TG,
                                      group_score_topk=gk)
-        keys = (O.sigmoid_f32(logits[0]) + bias).astype(np.float32)
+        keys = (O.sigmoid_key_f32(logits[0]) + bias).astype(np.float32)
         # group score: the best sum of any gk keys in the group, in fp32
         # (order-free for two terms)
         score = []
@@ -167,6 +167,28 @@ def test_group_limited_brute_force():
         groups = _brute_topk(np.array(score), TG, list(range(G)))
         eligible = sorted(e for g in groups for e in range(g * gs, (g + 1) * gs))
         assert idx[0].tolist() == _brute_topk(keys, k, eligible)
+
+
+def test_sigmoid_key_within_few_ulp_of_exact():
+    # dense grid over the whole clamp range plus random points
+    l = np.concatenate([np.linspace(-90, 90, 200001),
+                        np.random.default_rng(1).standard_normal(100000) * 4]
+                       ).astype(np.float32)
+    got = O.sigmoid_key_f32(l).astype(np.float64)
+    ref = scipy.special.expit(l.astype(np.float64))
+    ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
+    inside = np.abs(l) <= 87
+    assert (np.abs(got - ref)[inside] <= 4 * ulp[inside]).all()
+    # clamped tails stay within the clamp value's sigmoid
+    assert (got[l > 87] == 1.0).all()
+    assert (got[l < -88] <= scipy.special.expit(-88.0) * (1 + 1e-6)).all()
+    # monotone non-decreasing on the sorted grid
+    g = O.sigmoid_key_f32(np.sort(l))
+    assert (np.diff(g.astype(np.float64)) >= 0).all()
+    # the constants are the stated splits of ln 2
+    assert float(O._LN2_HI) + float(O._LN2_LO) == pytest.approx(
+        math.log(2.0), abs=1e-11)
+    assert int(np.float32(O._LN2_HI).view(np.uint32)) & 0xFFF == 0
 
 
 def test_sigmoid_bias_selects_but_does_not_weight():
