@@ -37,7 +37,7 @@ EXPORTED = ["moe_route_workspace_size", "moe_route",
             "moe_dispatch_layout_workspace_size", "moe_dispatch_layout",
             "moe_permute", "moe_grouped_ffn_workspace_size",
             "moe_grouped_ffn", "moe_combine", "moe_selftest_bounded_wait",
-            "moe_selftest_sigmoid_key",
+            "moe_selftest_sigmoid_key", "moe_dispatch_layout_noalloc",
             "moe_status_str", "moe_abi_version"]
 ABI_VERSION = 1
 
@@ -69,6 +69,9 @@ _SIGS = {
     "moe_dispatch_layout": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _vp,
                                    _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                    _sz, _vp, _vp]),
+    "moe_dispatch_layout_noalloc": (_i32, [_i32, _i32, _i32, _i32, _i32,
+                                           _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                           _vp, _vp, _vp, _vp]),
     "moe_permute": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "moe_grouped_ffn_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "moe_grouped_ffn": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
@@ -172,6 +175,20 @@ def moe_dispatch_layout(T, k, E, R, capacity, topk_idx, expert_counts,
         _p(n_dropped), _p(rank_send_counts), _p(rank_send_displs),
         _p(workspace), nbytes, _p(status), _stream(stream)),
         "moe_dispatch_layout")
+
+
+def moe_dispatch_layout_noalloc(T, k, E, R, capacity, topk_idx,
+                                expert_counts, expert_offsets, dst_row,
+                                src_pair, n_kept, n_dropped, rank_send_counts,
+                                rank_send_displs, status, stream=None):
+    """moe_dispatch_layout without a workspace argument: the library's
+    static 1 MiB device scratch is used instead, for callers that cannot
+    allocate device memory (see include/moe.h)."""
+    _check(load().moe_dispatch_layout_noalloc(
+        T, k, E, R, capacity, _p(topk_idx), _p(expert_counts),
+        _p(expert_offsets), _p(dst_row), _p(src_pair), _p(n_kept),
+        _p(n_dropped), _p(rank_send_counts), _p(rank_send_displs),
+        _p(status), _stream(stream)), "moe_dispatch_layout_noalloc")
 
 
 def moe_permute(T, k, D, dtype, x, dst_row, xp, stream=None):

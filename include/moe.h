@@ -173,6 +173,30 @@ MOE_API moe_status moe_dispatch_layout(int32_t T, int32_t k, int32_t E, int32_t 
                                void* workspace, size_t workspace_bytes,
                                int32_t* status, moe_stream_t stream);
 
+/* moe_dispatch_layout_noalloc -- moe_dispatch_layout for callers that
+ * cannot allocate device memory: a plugin inside a host engine that owns the
+ * whole device memory pool and passes it only input and output buffers, or
+ * a service that forbids cudaMalloc after start-up because an allocation
+ * can synchronise the device.  The pages have no counterpart; this is a
+ * deployment convenience.  Same arguments, outputs and results as
+ * moe_dispatch_layout, minus the workspace: the scratch is a static device
+ * array of MOE_NOALLOC_LAYOUT_SCRATCH_BYTES inside the library, held by
+ * every GPU that loads it until exit.
+ *  - Requires ceil(T*k / 2048) * E * 4 <= MOE_NOALLOC_LAYOUT_SCRATCH_BYTES,
+ *    else returns MOE_ERR_UNSUPPORTED without launching.
+ *  - The first call on each device (with that device current) looks up the
+ *    array's device address; make it before any stream capture.  A failed
+ *    lookup returns MOE_ERR_CUDA.
+ *  - All calls share the array; overlapping calls on the GPU (unordered
+ *    streams) race.  No cudaMalloc, cudaFree or other allocating call. */
+#define MOE_NOALLOC_LAYOUT_SCRATCH_BYTES (1u << 20)
+MOE_API moe_status moe_dispatch_layout_noalloc(
+    int32_t T, int32_t k, int32_t E, int32_t R, int32_t capacity,
+    const int32_t* topk_idx, int32_t* expert_counts, int32_t* expert_offsets,
+    int32_t* dst_row, int32_t* src_pair, int32_t* n_kept, int32_t* n_dropped,
+    int32_t* rank_send_counts, int32_t* rank_send_displs, int32_t* status,
+    moe_stream_t stream);
+
 /* moe_permute -- xp[dst_row[t*k + j]] = x[t] for every kept pair
  * ("Expert Parallelism in LLMs", The Execution Pipeline, step 2: tokens
  * physically reordered into contiguous per-destination buffers).  Each
