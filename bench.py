@@ -128,34 +128,73 @@ def build_layer(wl, device, seed):
     return layer, inp
 
 
-def launches_per_step(layer):
-    n = 2 + 3 + 1 + 1            # route (GEMM + select), layout, permute, combine
+def launches_per_step(layer, routed):
+    n = 3 + 1 + 1                # layout (3), permute, combine
+    if routed:
+        n += 2                   # route: router GEMM + select
     if not layer.identity:
         n += 2                   # grouped FFN: up and down projections
     return n
 
 
-def run_ours(args, rank, world, local_rank):
+def kernel_models(wl, n_kept, es, peaks):
+    """Algorithmic work of each step and the roofline time it implies.
+    Bytes count each input read once and each output written once;
+    intermediates (split-K partial logits, the SwiGLU activations H) are not
+    algorithmic."""
+    T, D, E, k, F = wl.T, wl.D, wl.E, wl.k, wl.F
+    P, N = T * k, n_kept
+    hbm = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops_sustained"] * 1e12
+    m = {}
+    m["route"] = dict(bytes=T * D * es + E * D * es + P * 8,
+                      flops=2.0 * T * D * E)
+    m["layout"] = dict(bytes=P * 4 + P * 4 + N * 4, flops=0.0)
+    m["permute"] = dict(bytes=T * D * es + N * D * es + P * 4, flops=0.0)
+    if not wl.identity_experts:
+        m["ffn"] = dict(bytes=E * 3 * F * D * es + 2 * N * D * es,
+                        flops=6.0 * D * F * N)
+    m["combine"] = dict(bytes=N * D * es + T * D * es + P * 8, flops=0.0)
+    for v in m.values():
+        t_hbm = v["bytes"] / hbm
+        t_tc = v["flops"] / tc if wl.dtype == "bf16" else 0.0
+        v["bound"] = "tensor" if t_tc > t_hbm else "hbm"
+        v["roofline_ms"] = max(t_hbm, t_tc) * 1e3
+    return m
+
+
+def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
     import torch
     from combine_router_gemm_top_b300 import workloads as W
     dist = None
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl")
+        if not dist.is_initialized():
+            dist.init_process_group("nccl")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    wl = W.WORKLOADS[args.workload]
+    wl = W.WORKLOADS[workload or args.workload]
     layer, inp = build_layer(wl, dev, wl.seed + rank)
     x = inp["x"]
+    idx_in = inp.get("topk_idx")      # pre-drawn routing (sweep workloads)
+    gate_in = inp.get("topk_gate")
     stream = torch.cuda.current_stream()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    names = ["route", "layout", "permute", "ffn", "combine"]
 
-    def step():
+    def step(m=None):
+        rec = (lambda j: m[j].record(stream)) if m else (lambda j: None)
+        rec(0)
         layer.route(x, stream)
-        layer.dispatch_layout(None, stream)
+        rec(1)
+        layer.dispatch_layout(idx_in, stream)
+        rec(2)
         layer.permute(x, stream)
+        rec(3)
         layer.grouped_ffn(stream)
-        layer.combine(None, None, stream)
+        rec(4)
+        layer.combine(gate_in, None, stream)
+        rec(5)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -171,33 +210,21 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.5)
     t_wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()
-        m = marks[i]
-        m[0].record(stream)
-        layer.route(x, stream)
-        m[1].record(stream)
-        layer.dispatch_layout(None, stream)
-        m[2].record(stream)
-        layer.permute(x, stream)
-        m[3].record(stream)
-        layer.grouped_ffn(stream)
-        m[4].record(stream)
-        layer.combine(None, None, stream)
-        m[5].record(stream)
+        step(marks[i])
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall0
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
 
-    parts = {"route": 0.0, "layout": 0.0, "permute": 0.0, "ffn": 0.0,
-             "combine": 0.0}
+    parts = dict.fromkeys(names, 0.0)
     total_ms = 0.0
     for m in marks:
-        for j, key in enumerate(parts):
+        for j, key in enumerate(names):
             parts[key] += m[j].elapsed_time(m[j + 1])
         total_ms += m[0].elapsed_time(m[5])
     if dist is not None:
@@ -209,16 +236,28 @@ def run_ours(args, rank, world, local_rank):
     x_host = x.cpu().pin_memory()
     y_host = torch.empty_like(layer.y, device="cpu").pin_memory()
     x_dev = torch.empty_like(x)
-    for _ in range(max(1, args.warmup)):
+    e2e_steps = max(1, min(args.steps, 200))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            x_dev.copy_(x_host, non_blocking=True)
+            layer.route(x_dev, stream)
+            layer.dispatch_layout(idx_in, stream)
+            layer.permute(x_dev, stream)
+            layer.grouped_ffn(stream)
+            layer.combine(gate_in, None, stream)
+            y_host.copy_(layer.y, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
         flush.zero_()
-        layer.forward_host(x_host, y_host, x_dev, stream)
+        e2e_step()
     torch.cuda.synchronize()
     e2e_ms = 0.0
-    for _ in range(args.steps):
+    for _ in range(e2e_steps):
         flush.zero_()
         a, b = ev(), ev()
         a.record(stream)
-        layer.forward_host(x_host, y_host, x_dev, stream)
+        e2e_step()
         b.record(stream)
         b.synchronize()
         e2e_ms += a.elapsed_time(b)
@@ -232,8 +271,6 @@ def run_ours(args, rank, world, local_rank):
     if status != 0:
         raise RuntimeError(f"device status {status}")
     if rank != 0:
-        if dist is not None:
-            dist.destroy_process_group()
         return None
 
     K = args.steps
@@ -241,39 +278,49 @@ def run_ours(args, rank, world, local_rank):
     peaks = load_peaks()
     tokens = wl.T * world * K
     value = tokens / (total_ms / 1e3)
-    ms_step = total_ms / K
-    pc_bytes = 2 * (wl.T * wl.D * es + n_kept * wl.D * es) + \
-        wl.T * wl.k * (4 + 4 + 4)
+    models = kernel_models(wl, n_kept, es, peaks)
+    kernels = {}
+    for key, mdl in models.items():
+        ms = parts[key] / K
+        if mdl["bound"] == "tensor":
+            ach, unit, pk = mdl["flops"] / (ms / 1e3) / 1e12, "TFLOP/s", \
+                peaks["bf16_tflops_sustained"]
+        else:
+            ach, unit, pk = mdl["bytes"] / (ms / 1e3) / 1e9, "GB/s", \
+                peaks["hbm_gbs"]
+        kernels[key] = {"ms": round(ms, 4), "bound": mdl["bound"],
+                        "achieved": round(ach, 1), "unit": unit,
+                        "frac": round(ach / pk, 4),
+                        "roofline_ms": round(mdl["roofline_ms"], 4)}
+        if mdl["flops"] and wl.dtype == "bf16":
+            kernels[key]["tflops"] = round(mdl["flops"] / (ms / 1e3) / 1e12, 1)
+    dom = max(kernels, key=lambda kk: kernels[kk]["ms"])
+    dk, dm = kernels[dom], models[dom]
+    if dk["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": dk["achieved"],
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": dk["frac"], "traffic": None,
+                "peak_note": "bf16 sustained (seconds-long loop), "
+                             + peaks["source"],
+                "frac_of_burst": round(dk["achieved"] / peaks["bf16_tflops"], 4),
+                "algorithmic_per_launch": dm["flops"]}
+    else:
+        roof = {"bound": "hbm", "achieved": dk["achieved"],
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dk["frac"],
+                "traffic": None, "peak_note": "HBM copy, " + peaks["source"],
+                "algorithmic_per_launch": dm["bytes"]}
+    roof["kernel"] = {"ffn": "moe_grouped_ffn (tcgen05 up + down launches)",
+                      "route": "moe_route (router GEMM + select)",
+                      "layout": "moe_dispatch_layout (3 launches)",
+                      "permute": "moe_permute", "combine": "moe_combine"}[dom]
+    pc_bytes = models["permute"]["bytes"] + models["combine"]["bytes"]
     pc_ms = (parts["permute"] + parts["combine"]) / K
     pc_gbs = pc_bytes / (pc_ms / 1e3) / 1e9
-    if layer.identity:
-        dom = "permute+combine"
-        achieved = pc_gbs
-        roof = {"bound": "hbm", "kernel": "moe_permute+moe_combine",
-                "achieved": round(achieved, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": None,
-                "algorithmic_bytes_per_step": pc_bytes}
-    else:
-        dom = "moe_grouped_ffn"
-        flops = 6.0 * wl.D * wl.F * n_kept
-        ffn_ms = parts["ffn"] / K
-        achieved = flops / (ffn_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"] if wl.dtype == "bf16" else None
-        roof = {"bound": "tensor", "kernel": "moe_grouped_ffn (tcgen05 up + "
-                "down launches)", "achieved": round(achieved, 2),
-                "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4) if peak else None,
-                "traffic": None, "peak_kind": "bf16 sustained, "
-                + peaks["source"],
-                "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
-                "algorithmic_flops_per_launch": flops}
-    e2e_tokens_s = tokens / (e2e_ms / 1e3)
+    e2e_tokens_s = wl.T * world * e2e_steps / (e2e_ms / 1e3)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "ms_per_step": round(total_ms / K, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == "bf16" else "f32",
         "data": "synthetic (seeded; random-init weights of the stated "
@@ -282,26 +329,26 @@ def run_ours(args, rank, world, local_rank):
                    "k": wl.k, "F": wl.F, "R": wl.R,
                    "capacity": layer.capacity or "dropless",
                    "score": wl.score, "n_kept": n_kept,
+                   "routing": wl.routing or "router",
                    "parallelism": f"replicas x{world}",
                    "l2": "flushed (256 MiB write) before every timed step"},
-        "per_step_ms": {k2: round(v / K, 4) for k2, v in parts.items()},
+        "kernels": kernels,
         "permute_combine": {"gbs": round(pc_gbs, 1),
                             "frac_of_hbm": round(pc_gbs / peaks["hbm_gbs"], 4),
                             "algorithmic_bytes": pc_bytes},
         "roofline": roof,
-        "dominant_kernel": dom,
         "e2e": {"value": round(e2e_tokens_s, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.T * wl.D * es,
                 "d2h_bytes_per_step": wl.T * wl.D * es},
-        "gpu_launches": launches_per_step(layer) * K,
+        "gpu_launches": launches_per_step(layer, True) * K,
         "clocks": clk,
         "wall_s_timed_loop": round(wall, 3),
     }
-    if dist is not None:
-        dist.destroy_process_group()
-    elif not args.no_cpu_baseline:
+    if world == 1 and cpu and not args.no_cpu_baseline:
         # the oracle on the host cores, fed the same (device) inputs
         line["cpu_baseline"] = run_cpu_baseline(wl, inp)
+    del layer, inp, flush
+    torch.cuda.empty_cache()
     return line
 
 
@@ -372,25 +419,33 @@ def run_cpu_baseline(wl, inp, steps=1):
                       f"combine), {s:.1f} s per pass"}
 
 
+REF_BUDGET_S = 150.0   # bound on the reference arm's timed work
+
+
 def run_reference(args, rank, world):
+    """The CPU oracle as it stands, on the host cores: each step is one
+    oracle pass over a bounded token sample of the workload.  If K such
+    steps would run past REF_BUDGET_S, only as many as fit are timed
+    (reported as steps_timed)."""
     if rank != 0:
         return None
     from combine_router_gemm_top_b300 import workloads as W
     wl = W.WORKLOADS[args.workload]
     inp = cpu_inputs(wl)
     n_tok = min(wl.T, REF_SAMPLE_TOKENS.get(wl.name, 64))
-    for _ in range(min(args.warmup, 1)):
-        oracle_sample_run(wl, inp, min(n_tok, 8))
-    secs = [oracle_sample_run(wl, inp, n_tok) for _ in range(args.steps)]
+    first = oracle_sample_run(wl, inp, n_tok)          # warm-up pass
+    steps = max(1, min(args.steps, int(REF_BUDGET_S / max(first, 1e-3))))
+    secs = [oracle_sample_run(wl, inp, n_tok) for _ in range(steps)]
     total = sum(secs)
-    value = n_tok * args.steps / total
+    value = n_tok * steps / total
     cb = {"value": round(value, 3), "unit": "tokens/s",
           "cores": cpu_threads(), "kind": "oracle",
-          "sample": f"first {n_tok} of {wl.T} tokens of {wl.name} per step"}
+          "sample": f"first {n_tok} of {wl.T} tokens of {wl.name} per step "
+                    f"(route, layout, permute, fp64 experts, combine)"}
     return {"impl": "reference", "metric": METRIC, "value": round(value, 3),
             "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup,
-            "ms_per_step": round(total / args.steps * 1e3, 1),
+            "steps_timed": steps, "warmup": args.warmup,
+            "ms_per_step": round(total / steps * 1e3, 1),
             "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": {"workload": wl.name, "T": wl.T, "D": wl.D, "E": wl.E,
@@ -404,11 +459,14 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="mixtral_bf16")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="dispatch/combine bandwidth sweep: one JSON line "
+                         "per (T, routing) identity-expert workload")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -422,11 +480,23 @@ def main():
         from combine_router_gemm_top_b300 import build as B
         if rank == 0:
             B.build(verbose=False)
+        if args.sweep:
+            for T in (4096, 16384, 65536):
+                for r in ("uniform", "zipf"):
+                    ln = run_ours(args, rank, world, local_rank,
+                                  workload=f"sweep_bf16_{r}_T{T}", cpu=False)
+                    if ln is not None:
+                        print(json.dumps(ln), flush=True)
+            return
         line = run_ours(args, rank, world, local_rank)
         if line is not None and "cpu_baseline" not in line:
             line["cpu_baseline"] = None
     if line is not None:
         print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
 
 
 if __name__ == "__main__":
