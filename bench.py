@@ -137,7 +137,7 @@ def launches_per_step(layer, routed):
     return n
 
 
-def kernel_models(wl, n_kept, es, peaks):
+def kernel_models(wl, n_kept, es, peaks, active_experts=None):
     """Algorithmic work of each step and the roofline time it implies.
     Bytes count each input read once and each output written once;
     intermediates (split-K partial logits, the SwiGLU activations H) are not
@@ -152,7 +152,8 @@ def kernel_models(wl, n_kept, es, peaks):
     m["layout"] = dict(bytes=P * 4 + P * 4 + N * 4, flops=0.0)
     m["permute"] = dict(bytes=T * D * es + N * D * es + P * 4, flops=0.0)
     if not wl.identity_experts:
-        m["ffn"] = dict(bytes=E * 3 * F * D * es + 2 * N * D * es,
+        ea = E if active_experts is None else active_experts
+        m["ffn"] = dict(bytes=ea * 3 * F * D * es + 2 * N * D * es,
                         flops=6.0 * D * F * N)
     m["combine"] = dict(bytes=N * D * es + T * D * es + P * 8, flops=0.0)
     for v in m.values():
@@ -174,6 +175,8 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     wl = W.WORKLOADS[workload or args.workload]
+    if args.tokens:
+        wl = wl.with_(T=args.tokens)
     layer, inp = build_layer(wl, dev, wl.seed + rank)
     x = inp["x"]
     idx_in = inp.get("topk_idx")      # pre-drawn routing (sweep workloads)
@@ -278,7 +281,8 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
     peaks = load_peaks()
     tokens = wl.T * world * K
     value = tokens / (total_ms / 1e3)
-    models = kernel_models(wl, n_kept, es, peaks)
+    active = int((layer.expert_counts > 0).sum().item())
+    models = kernel_models(wl, n_kept, es, peaks, active)
     kernels = {}
     for key, mdl in models.items():
         ms = parts[key] / K
@@ -329,6 +333,7 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
                    "k": wl.k, "F": wl.F, "R": wl.R,
                    "capacity": layer.capacity or "dropless",
                    "score": wl.score, "n_kept": n_kept,
+                   "active_experts": active,
                    "routing": wl.routing or "router",
                    "parallelism": f"replicas x{world}",
                    "l2": "flushed (256 MiB write) before every timed step"},
@@ -464,6 +469,9 @@ def main():
     ap.add_argument("--workload", default="mixtral_bf16")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count (small cases "
+                         "for profiler captures)")
     ap.add_argument("--sweep", action="store_true",
                     help="dispatch/combine bandwidth sweep: one JSON line "
                          "per (T, routing) identity-expert workload")
