@@ -177,6 +177,8 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
     wl = W.WORKLOADS[workload or args.workload]
     if args.tokens:
         wl = wl.with_(T=args.tokens)
+    if args.experts:
+        wl = wl.with_(E=args.experts, R=min(wl.R, args.experts))
     layer, inp = build_layer(wl, dev, wl.seed + rank)
     x = inp["x"]
     idx_in = inp.get("topk_idx")      # pre-drawn routing (sweep workloads)
@@ -471,6 +473,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count (small cases "
+                         "for profiler captures)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the workload's expert count (small cases "
                          "for profiler captures)")
     ap.add_argument("--sweep", action="store_true",
                     help="dispatch/combine bandwidth sweep: one JSON line "

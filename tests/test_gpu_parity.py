@@ -323,6 +323,7 @@ def run_ffn(xp, counts, w13, w2, F, sentinel=True):
 FFN_CASES = [
     # E, D, F, counts, dtype
     (4, 128, 256, [0, 1, 200, 129], torch.bfloat16),
+    (6, 256, 256, [255, 256, 257, 16, 17, 513], torch.bfloat16),
     (3, 256, 128, [128, 256, 5], torch.bfloat16),
     (1, 512, 384, [300], torch.bfloat16),
     (5, 192, 256, [7, 0, 0, 130, 64], torch.bfloat16),
