@@ -24,6 +24,13 @@
 //           H = SiLU(gate) * up rounded to bf16.
 //   kDown   grouped down-projection: B = 256 rows of W2, epilogue rounds to
 //           bf16.
+// Ragged tails (grouped modes): the last row block of an expert with at most
+// 112 rows runs with the operands swapped.  The same shared-memory tiles
+// feed two MMAs of shape 128 x n x 16, n = the tail rounded up to 16: the
+// weight halves of the B tile are the 128-row A operands and the token
+// tile is the n-row B operand.  TMEM then holds [feature, token] and the
+// epilogue writes transposed.  This cuts the MMA work spent on padding rows
+// from up to 127 rows per expert to at most 15.
 // Every wait is time-bounded (see mbar_wait); on expiry the CTA stops
 // issuing, drains its own copies and MMAs, frees TMEM, and reports
 // MOE_ERR_TIMEOUT.
@@ -78,6 +85,7 @@ struct TileInfo {
   int32_t out_col;    // first output column
   int32_t kb_begin, kb_end;
   int32_t split;      // route
+  int32_t swap_n;     // grouped tail: MMA N of the swapped form, 0 = normal
 };
 
 struct GemmShared {
@@ -107,6 +115,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a,
     ti.out_col = 0;
     ti.kb_begin = ti.split * a.kb_per_split;
     ti.kb_end = min(a.k_blocks, ti.kb_begin + a.kb_per_split);
+    ti.swap_n = 0;
     return ti;
   }
   // binary search: the expert whose tile range holds t
@@ -125,6 +134,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a,
   ti.split = 0;
   ti.a_row = row0 + m * kBM;
   ti.rows = min(kBM, cnt - m * kBM);
+  ti.swap_n = ti.rows <= kBM - 16 ? (ti.rows + 15) & ~15 : 0;
   ti.kb_begin = 0;
   ti.kb_end = a.k_blocks;
   if (MODE == kUp) {
@@ -148,6 +158,36 @@ template <int MODE>
 __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
                                              const TileInfo& ti,
                                              uint32_t tmem_row, int r) {
+  if (MODE != kRoute && ti.swap_n != 0) {
+    // swapped tail: TMEM lane r is output feature out_col + r (and, for the
+    // down projection, out_col + 128 + r); column j is token row a_row + j
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) +
+                         static_cast<int64_t>(ti.a_row) * a.out_ld +
+                         ti.out_col + r;
+    const int rows = min(ti.rows, a.M - ti.a_row);
+    const bool lo_ok = ti.out_col + r < a.out_cols;
+    const bool hi_ok = ti.out_col + 128 + r < a.out_cols;
+#pragma unroll 1
+    for (int c = 0; c < ti.swap_n; c += 16) {
+      float v0[16], v1[16];
+      tmem_ld16(tmem_row + c, v0);
+      tmem_ld16(tmem_row + 128 + c, v1);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int j = c + i;
+        if (j < rows) {
+          __nv_bfloat16* o = out + static_cast<int64_t>(j) * a.out_ld;
+          if (MODE == kUp) {
+            if (lo_ok) o[0] = __float2bfloat16_rn(silu_f32(v0[i]) * v1[i]);
+          } else {
+            if (lo_ok) o[0] = __float2bfloat16_rn(v0[i]);
+            if (hi_ok) o[128] = __float2bfloat16_rn(v1[i]);
+          }
+        }
+      }
+    }
+    return;
+  }
   const int64_t grow = static_cast<int64_t>(ti.a_row) + r;
   const bool valid = r < ti.rows && grow >= 0 && grow < a.M;
   if (MODE == kRoute) {
@@ -369,11 +409,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               smem_u32(b_tiles + static_cast<size_t>(stage) * b_tile_bytes);
           const uint64_t adesc = umma_desc_sw128(sa);
           const uint64_t bdesc = umma_desc_sw128(sb);
+          if (MODE == kRoute || ti.swap_n == 0) {
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k) {
-            // +32 bytes along K per step: +2 in the >>4 address field
-            umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
-                      (kb > ti.kb_begin || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kBK / kUmmaK; ++k) {
+              // +32 bytes along K per step: +2 in the >>4 address field
+              umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+                        (kb > ti.kb_begin || k > 0) ? 1u : 0u);
+            }
+          } else {
+            // swapped tail: each 128-row half of the weight tile is an A
+            // operand, the first swap_n token rows are the B operand
+            const uint32_t idesc_s = umma_idesc_bf16(kBM, ti.swap_n);
+            const uint64_t bdesc_hi = umma_desc_sw128(sb + 128 * 128);
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k) {
+              const uint32_t acc_in = (kb > ti.kb_begin || k > 0) ? 1u : 0u;
+              umma_bf16(d_tmem, bdesc + 2 * k, adesc + 2 * k, idesc_s, acc_in);
+              umma_bf16(d_tmem + 128, bdesc_hi + 2 * k, adesc + 2 * k, idesc_s,
+                        acc_in);
+            }
           }
           umma_commit(&sh.empty[stage]);
           if (++stage == a.stages) {

@@ -273,20 +273,23 @@ def dispatch_layout(topk_idx, E, R, capacity=None):
                 rank_send_displs=rank_displs)
 
 
-def dispatch_matrix(topk_idx, n_src, n_dst, E):
+def dispatch_matrix(topk_idx, n_src, n_dst, E, dst_row=None):
     """Pairs sent from each source shard to each destination rank: tokens
     are split into n_src equal contiguous shards, experts into n_dst
     contiguous blocks ("All-to-All Communication", the routing simulation
-    listing and its printed dispatch matrix)."""
+    listing and its printed dispatch matrix).  With dst_row given, only
+    kept pairs (dst_row >= 0) are counted: a dropped pair is never sent."""
     idx = np.asarray(topk_idx)
-    T = idx.shape[0]
+    T, k = idx.shape
     per_src = T // n_src
     epr = E // n_dst
     m = np.zeros((n_src, n_dst), dtype=np.int64)
     for t in range(T):
         s = t // per_src
-        for e in idx[t]:
-            m[s, int(e) // epr] += 1
+        for j in range(k):
+            if dst_row is not None and int(dst_row[t * k + j]) < 0:
+                continue
+            m[s, int(idx[t, j]) // epr] += 1
     return m
 
 
@@ -412,3 +415,106 @@ def dispatch_bytes_per_rank(T, k, D, ep, elem_bytes):
     Parallelism in LLMs", Communication Volume and Hardware Topology), for
     uniform routing."""
     return Fraction(T * k * D * (ep - 1) * elem_bytes, ep)
+
+
+# --------------------------------------------------------------------------
+# Router statistics ("Expert Parallelism in LLMs", Static Capacity Factors
+# and Token Dropping: the auxiliary load-balancing loss
+# L_aux = alpha * E * sum_i f_i * P_i; Modern Dropless Dynamic Dispatch:
+# dynamically adjusted bias terms on the routing scores).
+# --------------------------------------------------------------------------
+def router_probabilities(logits, mode):
+    """The router probability each token gives every expert, float64 [T, E].
+
+    softmax modes: p = softmax of the token's E logits.
+    sigmoid mode: p = s / sum over all E of s, with s = sigmoid(logit), the
+    scores normalised to a distribution over experts (reading: the pages
+    define P_i only as "the router probability allocated to expert i")."""
+    l64 = np.asarray(logits, dtype=np.float64)
+    out = np.zeros_like(l64)
+    for t in range(l64.shape[0]):
+        if mode == SIGMOID_BIAS:
+            s = sigmoid_f64(l64[t])
+            out[t] = s / s.sum()
+        else:
+            w = np.exp(l64[t] - l64[t].max())
+            out[t] = w / w.sum()
+    return out
+
+
+def router_stats(logits, topk_idx, E, mode, alpha):
+    """f_i, P_i and L_aux of one routing decision.
+
+      counts_routed[i] = pairs that selected expert i (before any capacity
+                         drop: "fraction of tokens dispatched" is read as
+                         the routing decision itself)
+      f_i = counts_routed[i] / (T * k)     (sums to 1)
+      P_i = mean over tokens of the router probability of expert i
+      L_aux = alpha * E * sum_i f_i * P_i
+    With perfectly even routing and even probabilities L_aux = alpha."""
+    idx = np.asarray(topk_idx)
+    T, k = idx.shape
+    counts = np.zeros(E, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            counts[int(idx[t, j])] += 1
+    f = counts / float(T * k) if T * k else np.zeros(E)
+    p = router_probabilities(logits, mode)
+    P = p.mean(axis=0) if T else np.zeros(E)
+    loss = alpha * E * float(np.sum(f * P))
+    return dict(counts_routed=counts, f=f, P=P, aux_loss=loss)
+
+
+def bias_update(bias, counts_routed, T, k, gamma):
+    """Auxiliary-loss-free balancing step on the selection bias: an expert
+    whose routed load is above the mean load T*k/E has its bias lowered by
+    gamma, one below it raised by gamma, one exactly at it left alone
+    (reading: the pages say only that the bias terms are adjusted
+    dynamically to keep the load balanced; this is the plainest rule that
+    moves every expert toward the mean).  The comparison is exact integer
+    arithmetic: sign(T*k - E*load)."""
+    b = np.asarray(bias, dtype=F32).copy()
+    E = b.shape[0]
+    for e in range(E):
+        d = T * k - E * int(counts_routed[e])
+        if d > 0:
+            b[e] = F32(b[e] + F32(gamma))
+        elif d < 0:
+            b[e] = F32(b[e] - F32(gamma))
+    return b
+
+
+# --------------------------------------------------------------------------
+# Static-capacity padded layout ("Expert Parallelism in LLMs", Static
+# Capacity Factors and Token Dropping: fixed per-expert buffers of
+# C_expert rows; unused slots are padding).
+# --------------------------------------------------------------------------
+def padded_layout(layout, E, capacity):
+    """Row of each kept pair in a [E, C, D] buffer: expert e owns rows
+    [e*C, (e+1)*C) and its kept pairs fill them in the compact layout's
+    order.  Returns dst_row_padded [P] (-1 if dropped), src_pair_padded
+    [E*C] (-1 for a padding row) and the uniform offsets e*C."""
+    cap = int(capacity)
+    dst = np.asarray(layout["dst_row"])
+    off = np.asarray(layout["offsets"])
+    src = np.asarray(layout["src_pair"])
+    counts = np.asarray(layout["counts"])
+    dst_p = np.full(dst.shape[0], -1, dtype=np.int64)
+    src_p = np.full(E * cap, -1, dtype=np.int64)
+    for e in range(E):
+        for pos in range(int(counts[e])):
+            p = int(src[int(off[e]) + pos])
+            dst_p[p] = e * cap + pos
+            src_p[e * cap + pos] = p
+    return dict(dst_row_padded=dst_p, src_pair_padded=src_p,
+                offsets_padded=np.arange(E + 1, dtype=np.int64) * cap)
+
+
+def permute_padded(x, src_pair_padded, k):
+    """xpad[r] = x[src_pair_padded[r] // k], zeros for padding rows."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.zeros((len(src_pair_padded), x.shape[1]))
+    for r, p in enumerate(src_pair_padded):
+        if int(p) >= 0:
+            out[r] = x[int(p) // k]
+    return out

@@ -329,6 +329,12 @@ FFN_CASES = [
     (5, 192, 256, [7, 0, 0, 130, 64], torch.bfloat16),
     (8, 1024, 512, [100, 300, 0, 17, 128, 129, 255, 1], torch.bfloat16),
     (8, 64, 128, [10, 50, 0, 3, 128, 70, 1, 250], torch.float32),
+    # tails of every swapped MMA width (16..112) and the 112/113 switch to
+    # the normal tile; D = 320 leaves a down-projection tile half outside D
+    (8, 256, 256, [16, 33, 112, 113, 128 + 48, 256 + 97, 240, 2],
+     torch.bfloat16),
+    (7, 320, 128, [40, 170, 3, 81, 128 + 65, 0, 97], torch.bfloat16),
+    (2, 768, 384, [1, 64], torch.bfloat16),
 ]
 
 
