@@ -164,6 +164,22 @@ def kernel_models(wl, n_kept, es, peaks, active_experts=None):
     return m
 
 
+def replica_seed(base_seed, rank):
+    """Each replica draws its own batch: weak scaling, no shared data."""
+    return base_seed + rank
+
+
+def max_over_ranks(value, device, dist=None):
+    """The slowest replica's time (the job finishes when it does); the
+    value itself with one process."""
+    import torch
+    if dist is None or not dist.is_initialized():
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
     import torch
     from combine_router_gemm_top_b300 import workloads as W
@@ -179,7 +195,7 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
         wl = wl.with_(T=args.tokens)
     if args.experts:
         wl = wl.with_(E=args.experts, R=min(wl.R, args.experts))
-    layer, inp = build_layer(wl, dev, wl.seed + rank)
+    layer, inp = build_layer(wl, dev, replica_seed(wl.seed, rank))
     x = inp["x"]
     idx_in = inp.get("topk_idx")      # pre-drawn routing (sweep workloads)
     gate_in = inp.get("topk_gate")
@@ -232,10 +248,7 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
         for j, key in enumerate(names):
             parts[key] += m[j].elapsed_time(m[j + 1])
         total_ms += m[0].elapsed_time(m[5])
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev, dist)
 
     # end to end through the public layer API from pinned host memory
     x_host = x.cpu().pin_memory()
@@ -266,10 +279,7 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
         b.record(stream)
         b.synchronize()
         e2e_ms += a.elapsed_time(b)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev, dist)
 
     n_kept = int(layer.n_kept.item())
     status = layer.device_status()
@@ -354,6 +364,133 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
     if world == 1 and cpu and not args.no_cpu_baseline:
         # the oracle on the host cores, fed the same (device) inputs
         line["cpu_baseline"] = run_cpu_baseline(wl, inp)
+    del layer, inp, flush
+    torch.cuda.empty_cache()
+    return line
+
+
+# ------------------------------------------------------- beyond the step
+def run_extras(args, local_rank, workload):
+    """Times the calls outside the five-step layer pass on one workload:
+    router statistics (L_aux, f, P), the bias step, the kept-pair dispatch
+    matrix and, for capacity workloads, the padded static-capacity path
+    (padded layout, pad fill, permute, grouped FFN and combine on E*C rows).
+    Each call is timed alone with CUDA events, after an L2 flush, median of
+    the repeats.  One JSON line per workload."""
+    import torch
+    from combine_router_gemm_top_b300 import _lib as L
+    from combine_router_gemm_top_b300 import workloads as W
+    from combine_router_gemm_top_b300.layer import MoELayer
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = W.WORKLOADS[workload]
+    inp = W.make_inputs(wl, device=dev, seed=wl.seed)
+    layer = MoELayer(wl.T, wl.D, wl.E, wl.k, wl.R, inp["w_r"], inp["w13"],
+                     inp["w2"], F=wl.F, score=wl.score,
+                     sel_bias=inp["sel_bias"],
+                     logit_offset=inp["logit_offset"],
+                     capacity_factor=wl.capacity_factor,
+                     n_groups=wl.n_groups, topk_groups=wl.topk_groups,
+                     group_score_topk=wl.group_score_topk, device=dev,
+                     keep_logits=True)
+    x = inp["x"]
+    layer.forward(x)
+    torch.cuda.synchronize()
+    peaks = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    T, D, E, k, P = wl.T, wl.D, wl.E, wl.k, wl.T * wl.k
+    es = x.element_size()
+    n_kept = int(layer.n_kept.item())
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    reps = max(5, min(args.steps, 50))
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = {}
+
+    def put(name, ms, nbytes=None, flops=None):
+        d = {"ms": round(ms, 4)}
+        if nbytes is not None:
+            gbs = nbytes / (ms / 1e3) / 1e9
+            d.update(bytes=nbytes, gbs=round(gbs, 1), bound="hbm",
+                     frac_of_hbm=round(gbs / hbm, 4))
+        if flops is not None:
+            tf = flops / (ms / 1e3) / 1e12
+            d.update(flops=flops, tflops=round(tf, 1), bound="tensor",
+                     frac_of_sustained=round(
+                         tf / peaks["bf16_tflops_sustained"], 4))
+        out[name] = d
+
+    st = torch.zeros(1, **i32)
+    ws = torch.empty(L.moe_router_stats_workspace_size(T, E),
+                     dtype=torch.uint8, device=dev)
+    f = torch.empty(E, dtype=torch.float32, device=dev)
+    Pm = torch.empty(E, dtype=torch.float32, device=dev)
+    cnt = torch.empty(E, **i32)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    put("router_stats", timed(lambda: L.moe_router_stats(
+        T, E, k, wl.score, layer.logits, layer.topk_idx, 0.01, f, Pm, cnt,
+        loss, ws, st)), nbytes=T * E * 4 + P * 4)
+    bias = torch.zeros(E, dtype=torch.float32, device=dev)
+    put("router_bias_update", timed(lambda: L.moe_router_bias_update(
+        T, k, E, cnt, 1e-3, bias)), nbytes=E * 12)
+    R = wl.R
+    mat = torch.empty(R * R, **i32)
+    put("dispatch_matrix", timed(lambda: L.moe_dispatch_matrix(
+        T, k, E, R, R, layer.topk_idx, layer.dst_row, mat, st)),
+        nbytes=2 * P * 4)
+    cap = layer.capacity
+    if cap > 0 and not layer.identity:
+        rows = E * cap
+        dst_p = torch.empty(P, **i32)
+        off_p = torch.empty(E + 1, **i32)
+        xpad = torch.empty((rows, D), dtype=x.dtype, device=dev)
+        ypad = torch.empty_like(xpad)
+        fws = torch.empty(L.moe_grouped_ffn_workspace_size(
+            E, D, wl.F, rows, layer.dcode), dtype=torch.uint8, device=dev)
+        y = torch.empty_like(x)
+        put("padded_layout", timed(lambda: L.moe_padded_layout(
+            T, k, E, cap, layer.topk_idx, layer.dst_row,
+            layer.expert_offsets, dst_p, off_p, st)), nbytes=3 * P * 4)
+        put("pad_fill", timed(lambda: L.moe_pad_fill(
+            E, cap, D, layer.dcode, layer.expert_counts, xpad)),
+            nbytes=(rows - n_kept) * D * es)
+        put("padded_permute", timed(lambda: L.moe_permute(
+            T, k, D, layer.dcode, x, dst_p, xpad)),
+            nbytes=T * D * es + n_kept * D * es + P * 4)
+        put("padded_ffn", timed(lambda: L.moe_grouped_ffn(
+            E, D, wl.F, rows, layer.dcode, xpad, off_p, layer.w13, layer.w2,
+            ypad, fws, st)), flops=6.0 * D * wl.F * rows)
+        put("padded_combine", timed(lambda: L.moe_combine(
+            T, k, D, layer.dcode, ypad, dst_p, layer.topk_gate, y)),
+            nbytes=n_kept * D * es + T * D * es + P * 8)
+    torch.cuda.synchronize()
+    if st.item() != 0 or layer.device_status() != 0:
+        raise RuntimeError("device status set during the extras")
+    line = {"mode": "extras", "workload": wl.name,
+            "config": {"T": T, "D": D, "E": E, "k": k, "F": wl.F, "R": R,
+                       "capacity": cap or "dropless", "n_kept": n_kept},
+            "repeats": reps, "timing": "CUDA events per call, L2 flushed, "
+                                       "median",
+            "peaks": {"hbm_gbs": hbm,
+                      "bf16_tflops_sustained": peaks["bf16_tflops_sustained"],
+                      "source": peaks["source"]},
+            "kernels": out}
     del layer, inp, flush
     torch.cuda.empty_cache()
     return line
@@ -477,6 +614,10 @@ def main():
     ap.add_argument("--experts", type=int, default=0,
                     help="override the workload's expert count (small cases "
                          "for profiler captures)")
+    ap.add_argument("--extras", action="store_true",
+                    help="time router statistics, the bias step, the "
+                         "dispatch matrix and the padded static-capacity "
+                         "path: one JSON line per workload")
     ap.add_argument("--sweep", action="store_true",
                     help="dispatch/combine bandwidth sweep: one JSON line "
                          "per (T, routing) identity-expert workload")
@@ -493,6 +634,13 @@ def main():
         from combine_router_gemm_top_b300 import build as B
         if rank == 0:
             B.build(verbose=False)
+        if args.extras:
+            if rank == 0:
+                for name in ("switch_bf16", "deepseek_bf16", "mixtral_bf16",
+                             "tiny_f32"):
+                    print(json.dumps(run_extras(args, local_rank, name)),
+                          flush=True)
+            return
         if args.sweep:
             for T in (4096, 16384, 65536):
                 for r in ("uniform", "zipf"):

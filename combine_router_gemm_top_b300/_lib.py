@@ -38,6 +38,9 @@ EXPORTED = ["moe_route_workspace_size", "moe_route",
             "moe_permute", "moe_grouped_ffn_workspace_size",
             "moe_grouped_ffn", "moe_combine", "moe_selftest_bounded_wait",
             "moe_selftest_sigmoid_key", "moe_dispatch_layout_noalloc",
+            "moe_router_stats_workspace_size", "moe_router_stats",
+            "moe_router_bias_update", "moe_dispatch_matrix",
+            "moe_padded_layout", "moe_pad_fill",
             "moe_status_str", "moe_abi_version"]
 ABI_VERSION = 1
 
@@ -77,6 +80,17 @@ _SIGS = {
     "moe_grouped_ffn": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
                                _vp, _vp, _vp, _sz, _vp, _vp]),
     "moe_combine": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "moe_router_stats_workspace_size": (_sz, [_i32, _i32]),
+    "moe_router_stats": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp,
+                                ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _sz,
+                                _vp, _vp]),
+    "moe_router_bias_update": (_i32, [_i32, _i32, _i32, _vp, ctypes.c_float,
+                                      _vp, _vp]),
+    "moe_dispatch_matrix": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _vp,
+                                   _vp, _vp, _vp]),
+    "moe_padded_layout": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
+                                 _vp, _vp, _vp]),
+    "moe_pad_fill": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_selftest_bounded_wait": (_i32, [_vp, _u64, _vp]),
     "moe_selftest_sigmoid_key": (_i32, [_vp, _vp, _i32, _vp]),
     "moe_status_str": (ctypes.c_char_p, [_i32]),
@@ -213,6 +227,50 @@ def moe_combine(T, k, D, dtype, yp, dst_row, topk_gate, y, stream=None):
     _check(load().moe_combine(T, k, D, dtype, _p(yp), _p(dst_row),
                               _p(topk_gate), _p(y), _stream(stream)),
            "moe_combine")
+
+
+def moe_router_stats_workspace_size(T, E) -> int:
+    return load().moe_router_stats_workspace_size(T, E)
+
+
+def moe_router_stats(T, E, k, score, logits, topk_idx, alpha, f, P,
+                     counts_routed, aux_loss, workspace, status, stream=None):
+    if isinstance(score, str):
+        score = SCORE_CODES[score]
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().moe_router_stats(T, E, k, score, _p(logits), _p(topk_idx),
+                                   float(alpha), _p(f), _p(P),
+                                   _p(counts_routed), _p(aux_loss),
+                                   _p(workspace), nbytes, _p(status),
+                                   _stream(stream)), "moe_router_stats")
+
+
+def moe_router_bias_update(T, k, E, counts_routed, gamma, bias, stream=None):
+    _check(load().moe_router_bias_update(T, k, E, _p(counts_routed),
+                                         float(gamma), _p(bias),
+                                         _stream(stream)),
+           "moe_router_bias_update")
+
+
+def moe_dispatch_matrix(T, k, E, n_src, n_dst, topk_idx, dst_row, matrix,
+                        status, stream=None):
+    _check(load().moe_dispatch_matrix(T, k, E, n_src, n_dst, _p(topk_idx),
+                                      _p(dst_row), _p(matrix), _p(status),
+                                      _stream(stream)), "moe_dispatch_matrix")
+
+
+def moe_padded_layout(T, k, E, capacity, topk_idx, dst_row, expert_offsets,
+                      dst_row_padded, offsets_padded, status, stream=None):
+    _check(load().moe_padded_layout(T, k, E, capacity, _p(topk_idx),
+                                    _p(dst_row), _p(expert_offsets),
+                                    _p(dst_row_padded), _p(offsets_padded),
+                                    _p(status), _stream(stream)),
+           "moe_padded_layout")
+
+
+def moe_pad_fill(E, capacity, D, dtype, expert_counts, buf, stream=None):
+    _check(load().moe_pad_fill(E, capacity, D, dtype, _p(expert_counts),
+                               _p(buf), _stream(stream)), "moe_pad_fill")
 
 
 def moe_selftest_bounded_wait(status, limit_ns, stream=None):

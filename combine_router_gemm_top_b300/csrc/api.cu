@@ -238,6 +238,91 @@ moe_status moe_grouped_ffn(int32_t E, int32_t D, int32_t F, int32_t max_rows,
                             reinterpret_cast<cudaStream_t>(stream), num_sms());
 }
 
+size_t moe_router_stats_workspace_size(int32_t T, int32_t E) {
+  if (T < 0 || E < 1 || E > 256) return 0;
+  return router_stats_ws_bytes(T, E);
+}
+
+moe_status moe_router_stats(int32_t T, int32_t E, int32_t k, int32_t score,
+                            const float* logits, const int32_t* topk_idx,
+                            float alpha, float* f, float* P,
+                            int32_t* counts_routed, float* aux_loss,
+                            void* workspace, size_t workspace_bytes,
+                            int32_t* status, moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > 256 || k < 1 || k > E || k > 32)
+    return MOE_ERR_INVALID;
+  if (score < MOE_SCORE_SOFTMAX_TOPK || score > MOE_SCORE_SIGMOID_BIAS)
+    return MOE_ERR_INVALID;
+  if (static_cast<int64_t>(T) * E > INT32_MAX) return MOE_ERR_INVALID;
+  if (f == nullptr || P == nullptr || aux_loss == nullptr ||
+      workspace == nullptr)
+    return MOE_ERR_INVALID;
+  if (T > 0 && (logits == nullptr || topk_idx == nullptr))
+    return MOE_ERR_INVALID;
+  if (!aligned(workspace, 16) || workspace_bytes < router_stats_ws_bytes(T, E))
+    return MOE_ERR_INVALID;
+  return launch_router_stats(T, E, k, score, logits, topk_idx, alpha, f, P,
+                             counts_routed, aux_loss, workspace, status,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_router_bias_update(int32_t T, int32_t k, int32_t E,
+                                  const int32_t* counts_routed, float gamma,
+                                  float* bias, moe_stream_t stream) {
+  if (T < 0 || k < 1 || E < 1 || counts_routed == nullptr || bias == nullptr)
+    return MOE_ERR_INVALID;
+  return launch_router_bias_update(T, E, k, gamma, counts_routed, bias,
+                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_dispatch_matrix(int32_t T, int32_t k, int32_t E, int32_t n_src,
+                               int32_t n_dst, const int32_t* topk_idx,
+                               const int32_t* dst_row, int32_t* matrix,
+                               int32_t* status, moe_stream_t stream) {
+  if (T < 0 || k < 1 || k > 32 || E < 1 || n_src < 1 || n_dst < 1 ||
+      n_dst > 4096 || E % n_dst != 0)
+    return MOE_ERR_INVALID;
+  if (T % n_src != 0 || static_cast<int64_t>(T) * k > INT32_MAX)
+    return MOE_ERR_INVALID;
+  if (static_cast<int64_t>(n_src) * n_dst > INT32_MAX || n_src > 65535)
+    return MOE_ERR_INVALID;
+  if (matrix == nullptr || (T > 0 && topk_idx == nullptr))
+    return MOE_ERR_INVALID;
+  return launch_dispatch_matrix(T, k, E, n_src, n_dst, topk_idx, dst_row,
+                                matrix, status,
+                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_padded_layout(int32_t T, int32_t k, int32_t E, int32_t capacity,
+                             const int32_t* topk_idx, const int32_t* dst_row,
+                             const int32_t* expert_offsets,
+                             int32_t* dst_row_padded, int32_t* offsets_padded,
+                             int32_t* status, moe_stream_t stream) {
+  if (T < 0 || k < 1 || k > 32 || E < 1 || capacity < 1) return MOE_ERR_INVALID;
+  if (static_cast<int64_t>(E) * capacity > INT32_MAX ||
+      static_cast<int64_t>(T) * k > INT32_MAX)
+    return MOE_ERR_INVALID;
+  if (expert_offsets == nullptr || offsets_padded == nullptr)
+    return MOE_ERR_INVALID;
+  if (T > 0 && (topk_idx == nullptr || dst_row == nullptr ||
+                dst_row_padded == nullptr))
+    return MOE_ERR_INVALID;
+  return launch_padded_layout(T, k, E, capacity, topk_idx, dst_row,
+                              expert_offsets, dst_row_padded, offsets_padded,
+                              status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_pad_fill(int32_t E, int32_t capacity, int32_t D, int32_t dtype,
+                        const int32_t* expert_counts, void* buf,
+                        moe_stream_t stream) {
+  if (E < 1 || capacity < 1 || !rows_ok(1, 1, D, dtype)) return MOE_ERR_INVALID;
+  if (static_cast<int64_t>(E) * capacity > INT32_MAX) return MOE_ERR_INVALID;
+  if (expert_counts == nullptr || buf == nullptr || !aligned(buf, 16))
+    return MOE_ERR_INVALID;
+  return launch_pad_fill(E, capacity, D, dtype, expert_counts, buf,
+                         reinterpret_cast<cudaStream_t>(stream), num_sms());
+}
+
 moe_status moe_selftest_bounded_wait(int32_t* status, uint64_t limit_ns,
                                      moe_stream_t stream) {
   if (status == nullptr) return MOE_ERR_INVALID;

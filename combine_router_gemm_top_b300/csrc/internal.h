@@ -72,6 +72,30 @@ moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
                               void* ws, int32_t* status, cudaStream_t stream,
                               int num_sms);
 
+size_t router_stats_ws_bytes(int T, int E);
+moe_status launch_router_stats(int T, int E, int k, int score,
+                               const float* logits, const int32_t* topk_idx,
+                               float alpha, float* f, float* P,
+                               int32_t* counts_routed, float* aux_loss,
+                               void* ws, int32_t* status, cudaStream_t stream);
+moe_status launch_router_bias_update(int T, int E, int k, float gamma,
+                                     const int32_t* counts, float* bias,
+                                     cudaStream_t stream);
+moe_status launch_dispatch_matrix(int T, int k, int E, int n_src, int n_dst,
+                                  const int32_t* topk_idx,
+                                  const int32_t* dst_row, int32_t* matrix,
+                                  int32_t* status, cudaStream_t stream);
+moe_status launch_padded_layout(int T, int k, int E, int capacity,
+                                const int32_t* topk_idx,
+                                const int32_t* dst_row,
+                                const int32_t* offsets,
+                                int32_t* dst_row_padded,
+                                int32_t* offsets_padded, int32_t* status,
+                                cudaStream_t stream);
+moe_status launch_pad_fill(int E, int capacity, int D, int dtype,
+                           const int32_t* counts, void* buf,
+                           cudaStream_t stream, int num_sms);
+
 moe_status launch_sigmoid_key(const float* l, float* out, int n,
                               cudaStream_t stream);
 moe_status launch_selftest_wait(int32_t* status, uint64_t limit_ns,

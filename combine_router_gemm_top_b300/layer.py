@@ -39,7 +39,8 @@ class MoELayer:
     def __init__(self, T, D, E, k, R, w_r, w13=None, w2=None, F=0,
                  score="softmax_topk", sel_bias=None, logit_offset=None,
                  capacity_factor=None, n_groups=1, topk_groups=1,
-                 group_score_topk=0, device=None, keep_logits=False):
+                 group_score_topk=0, device=None, keep_logits=False,
+                 padded=False):
         L.load()
         self.device = torch.device(device or w_r.device)
         self.dtype = w_r.dtype
@@ -80,6 +81,23 @@ class MoELayer:
                 E, D, F, P, self.dcode))
         self.y = torch.empty((T, D), dtype=self.dtype, device=dev)
         self.status = torch.zeros(1, **i32)
+        # static-capacity [E, C, D] buffers ("Static Capacity Factors and
+        # Token Dropping"): every expert owns C rows, padding rows are zero
+        self.padded = bool(padded)
+        if self.padded:
+            if self.capacity <= 0:
+                raise ValueError("the padded layout needs a capacity factor")
+            rows = E * self.capacity
+            self.dst_row_padded = torch.empty(P, **i32)
+            self.offsets_padded = torch.empty(E + 1, **i32)
+            self.xpad = torch.empty((max(rows, 1), D), dtype=self.dtype,
+                                    device=dev)
+            self.ypad = self.xpad if self.identity else torch.empty_like(
+                self.xpad)
+            if not self.identity:
+                self.ffn_ws_padded = self._bytes(
+                    L.moe_grouped_ffn_workspace_size(E, D, F, rows,
+                                                     self.dcode))
 
     def _bytes(self, n):
         # 256-byte aligned scratch (torch's allocator aligns to >= 512 B)
@@ -118,11 +136,48 @@ class MoELayer:
                       self.dst_row, gate, out, stream)
         return out
 
+    # ---------------------------------------------------------- padded
+    def padded_layout(self, topk_idx=None, stream=None):
+        """Rows of the [E, C, D] buffer for the kept pairs, then zeros in
+        the padding rows (moe_padded_layout, moe_pad_fill)."""
+        idx = self.topk_idx if topk_idx is None else topk_idx
+        L.moe_padded_layout(self.T, self.k, self.E, self.capacity, idx,
+                            self.dst_row, self.expert_offsets,
+                            self.dst_row_padded, self.offsets_padded,
+                            self.status, stream)
+        L.moe_pad_fill(self.E, self.capacity, self.D, self.dcode,
+                       self.expert_counts, self.xpad, stream)
+
+    def forward_padded(self, x, topk_idx=None, topk_gate=None, y=None,
+                       stream=None):
+        """The layer on the static-capacity layout: every expert computes
+        all of its C rows (padding rows are zero in and zero out)."""
+        if topk_idx is None:
+            self.route(x, stream)
+        self.dispatch_layout(topk_idx, stream)
+        self.padded_layout(topk_idx, stream)
+        L.moe_permute(self.T, self.k, self.D, self.dcode, x,
+                      self.dst_row_padded, self.xpad, stream)
+        if not self.identity:
+            L.moe_grouped_ffn(self.E, self.D, self.F,
+                              self.E * self.capacity, self.dcode, self.xpad,
+                              self.offsets_padded, self.w13, self.w2,
+                              self.ypad, self.ffn_ws_padded, self.status,
+                              stream)
+        gate = self.topk_gate if topk_gate is None else topk_gate
+        out = self.y if y is None else y
+        L.moe_combine(self.T, self.k, self.D, self.dcode, self.ypad,
+                      self.dst_row_padded, gate, out, stream)
+        return out
+
     # ---------------------------------------------------------- layer
     def forward(self, x, topk_idx=None, topk_gate=None, y=None, stream=None):
         """y = MoE(x) for x [T, D] on the device.  With topk_idx/topk_gate
         given, routing is taken from them (pre-drawn routing) and moe_route
-        is skipped."""
+        is skipped.  A layer built with padded=True runs the static-capacity
+        layout."""
+        if self.padded:
+            return self.forward_padded(x, topk_idx, topk_gate, y, stream)
         if topk_idx is None:
             self.route(x, stream)
         self.dispatch_layout(topk_idx, stream)

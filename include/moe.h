@@ -248,6 +248,116 @@ MOE_API moe_status moe_combine(int32_t T, int32_t k, int32_t D, int32_t dtype,
                        const void* yp, const int32_t* dst_row,
                        const float* topk_gate, void* y, moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Router statistics and load balancing
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of scratch moe_router_stats needs (per-block partial sums).
+ * Returns 0 for invalid sizes. */
+MOE_API size_t moe_router_stats_workspace_size(int32_t T, int32_t E);
+
+/* moe_router_stats -- the auxiliary load-balancing loss of one routing
+ * decision ("Expert Parallelism in LLMs", Static Capacity Factors and Token
+ * Dropping: L_aux = alpha * E * sum_i f_i * P_i, f_i the fraction of tokens
+ * dispatched to expert i, P_i the router probability allocated to it).
+ *   score          moe_score of the routing: the router probability of a
+ *                  token is the softmax of its E logits (softmax modes) or
+ *                  its E sigmoid scores normalised to sum to 1 (sigmoid
+ *                  mode)
+ *   logits         [T, E] fp32 in: the logits selection used (moe_route's
+ *                  logits_out)
+ *   topk_idx       [T, k] int32 in: the routing decision
+ *   f              [E] fp32 out: routed pairs of expert i / (T*k), counted
+ *                  before any capacity drop
+ *   P              [E] fp32 out: mean over the T tokens of the router
+ *                  probability of expert i
+ *   counts_routed  [E] int32 out or NULL: routed pairs per expert
+ *   aux_loss       [1] fp32 out: alpha * E * sum_i f_i P_i
+ *   workspace      >= moe_router_stats_workspace_size(T, E) bytes, 16-byte
+ *                  aligned
+ * Probabilities are evaluated in fp32 and summed in fp64 in a fixed order:
+ * the results are deterministic.  Ids outside [0, E) are skipped and raise
+ * MOE_ERR_INDEX in `status`.  E <= 256, 1 <= k <= min(E, 32). */
+MOE_API moe_status moe_router_stats(int32_t T, int32_t E, int32_t k,
+                                    int32_t score, const float* logits,
+                                    const int32_t* topk_idx, float alpha,
+                                    float* f, float* P, int32_t* counts_routed,
+                                    float* aux_loss, void* workspace,
+                                    size_t workspace_bytes, int32_t* status,
+                                    moe_stream_t stream);
+
+/* moe_router_bias_update -- one step of auxiliary-loss-free balancing on the
+ * selection bias of MOE_SCORE_SIGMOID_BIAS ("Expert Parallelism in LLMs",
+ * Modern Dropless Dynamic Dispatch: bias terms on the routing scores,
+ * adjusted dynamically to keep the experts' load balanced).  The pages do
+ * not give the rule; this is the plainest one that moves every expert
+ * toward the mean load T*k/E:
+ *     bias[e] += gamma  if counts_routed[e] * E < T * k   (underloaded)
+ *     bias[e] -= gamma  if counts_routed[e] * E > T * k   (overloaded)
+ * (exact integer comparison, one fp32 add per expert).
+ *   counts_routed  [E] int32 in (moe_router_stats' output)
+ *   bias           [E] fp32 in/out */
+MOE_API moe_status moe_router_bias_update(int32_t T, int32_t k, int32_t E,
+                                          const int32_t* counts_routed,
+                                          float gamma, float* bias,
+                                          moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Dispatch bookkeeping beyond the compact layout
+ * ------------------------------------------------------------------------ */
+
+/* moe_dispatch_matrix -- pairs sent from each virtual source device to each
+ * virtual destination device ("All-to-All Communication", the routing
+ * simulation listing and its printed dispatch matrix: rows = source device,
+ * columns = destination device).  Tokens form n_src equal contiguous shards
+ * (token t is on source t / (T / n_src)); experts form n_dst contiguous
+ * blocks (expert e lives on destination e / (E / n_dst)).
+ *   topk_idx  [T*k] int32 in
+ *   dst_row   [T*k] int32 in or NULL: with it, dropped pairs (dst_row < 0)
+ *             are not counted; with NULL every routed pair is
+ *   matrix    [n_src, n_dst] int32 out (row-major)
+ * Requires T % n_src == 0, E % n_dst == 0, n_dst <= 4096.  Row sums are the
+ * pairs each source sends; column sums equal moe_dispatch_layout's
+ * rank_send_counts when n_dst = R.  Ids outside [0, E) are skipped and raise
+ * MOE_ERR_INDEX.  Exact (integer) and deterministic. */
+MOE_API moe_status moe_dispatch_matrix(int32_t T, int32_t k, int32_t E,
+                                       int32_t n_src, int32_t n_dst,
+                                       const int32_t* topk_idx,
+                                       const int32_t* dst_row, int32_t* matrix,
+                                       int32_t* status, moe_stream_t stream);
+
+/* moe_padded_layout -- rows of the static-capacity buffer [E, C, D]
+ * ("Expert Parallelism in LLMs", Static Capacity Factors and Token Dropping:
+ * each expert owns a fixed buffer of C_expert rows; empty slots are
+ * padding).  Expert e owns rows [e*C, (e+1)*C) and its kept pairs fill them
+ * in the compact layout's order:
+ *     dst_row_padded[p] = e*C + (dst_row[p] - expert_offsets[e]), or -1
+ *     offsets_padded[e] = e*C, e = 0..E
+ * The inputs are moe_dispatch_layout's outputs for the same capacity C.
+ * moe_permute and moe_combine take dst_row_padded in place of dst_row, and
+ * moe_grouped_ffn takes offsets_padded with max_rows = E*C (a padding row
+ * is zero after moe_pad_fill, and SwiGLU maps it to zero).
+ *   topk_idx, dst_row  [T*k] int32 in; expert_offsets [E+1] int32 in
+ *   dst_row_padded     [T*k] int32 out; offsets_padded [E+1] int32 out
+ * Requires capacity >= 1 and E * capacity <= INT32_MAX.  A kept row outside
+ * its expert's C slots raises MOE_ERR_INDEX and is marked -1. */
+MOE_API moe_status moe_padded_layout(int32_t T, int32_t k, int32_t E,
+                                     int32_t capacity, const int32_t* topk_idx,
+                                     const int32_t* dst_row,
+                                     const int32_t* expert_offsets,
+                                     int32_t* dst_row_padded,
+                                     int32_t* offsets_padded, int32_t* status,
+                                     moe_stream_t stream);
+
+/* moe_pad_fill -- zero the padding rows of a padded buffer: rows
+ * [e*C + expert_counts[e], (e+1)*C) of buf [E*C, D] for every expert; rows
+ * holding kept pairs are not touched.
+ *   expert_counts [E] int32 in (kept counts, each <= C)
+ *   buf           [E*C, D] dtype in/out, 16-byte aligned */
+MOE_API moe_status moe_pad_fill(int32_t E, int32_t capacity, int32_t D,
+                                int32_t dtype, const int32_t* expert_counts,
+                                void* buf, moe_stream_t stream);
+
 /* Test hook for the bounded-wait machinery: launches one CTA that waits on
  * a shared-memory barrier nothing arrives on, gives up after `limit_ns`
  * nanoseconds, writes MOE_ERR_TIMEOUT into `status` and returns. */
