@@ -518,3 +518,138 @@ def permute_padded(x, src_pair_padded, k):
         if int(p) >= 0:
             out[r] = x[int(p) // k]
     return out
+
+
+# --------------------------------------------------------------------------
+# Backward pass ("Expert Parallelism in LLMs", Backward Pass Symmetry: the
+# upstream gradient dL/dy goes to the experts along the dispatch pattern,
+# the experts form their weight gradients and input gradients, and the
+# input gradients return along the combine pattern).  The routing decision
+# (which experts, which pairs are kept) is piecewise constant in x, so the
+# gradient flows through the gates and the experts with the selection
+# fixed; that is the plain chain rule of the layer equation
+#     y_t = sum over kept slots j of g_j(x_t) * Expert_{e_j}(x_t).
+# --------------------------------------------------------------------------
+def silu_grad(z):
+    """d/dz [z * sigmoid(z)] = sigmoid(z) * (1 + z * (1 - sigmoid(z)))."""
+    s = 1.0 / (1.0 + np.exp(-z))
+    return s * (1.0 + z * (1.0 - s))
+
+
+def expert_backward(h, w1, w3, w2, dout):
+    """Gradients of out = W2 (SiLU(W1 h) * (W3 h)) for rows h [n, D] given
+    dout [n, D]: returns dh [n, D], dw1, dw3 [F, D], dw2 [D, F]."""
+    h = np.asarray(h, dtype=np.float64)
+    w1, w3, w2 = (np.asarray(w, dtype=np.float64) for w in (w1, w3, w2))
+    dout = np.asarray(dout, dtype=np.float64)
+    g = h @ w1.T
+    u = h @ w3.T
+    act = silu(g) * u
+    dact = dout @ w2                      # [n, F]
+    dw2 = dout.T @ act                    # [D, F]
+    du = dact * silu(g)
+    dg = dact * u * silu_grad(g)
+    dh = dg @ w1 + du @ w3
+    dw1 = dg.T @ h
+    dw3 = du.T @ h
+    return dh, dw1, dw3, dw2
+
+
+def gate_backward(logits_row, sel, dgate, mode):
+    """dL/dlogits of one token from dL/dgate of its k selected slots.
+
+      softmax_topk: g = softmax over the selected logits
+      softmax_full: g_j = p_{e_j}, p = softmax over all E logits
+      sigmoid_bias: g_j = s_j / sum_sel s, s = sigmoid(logit) (the bias
+                    only selects, so it has no gradient path)
+    """
+    l = np.asarray(logits_row, dtype=np.float64)
+    dgate = np.asarray(dgate, dtype=np.float64)
+    dl = np.zeros_like(l)
+    sel = [int(e) for e in sel]
+    if mode == SOFTMAX_TOPK:
+        z = l[sel]
+        w = np.exp(z - z.max())
+        g = w / w.sum()
+        dl[sel] = g * (dgate - float(g @ dgate))
+    elif mode == SOFTMAX_FULL:
+        w = np.exp(l - l.max())
+        p = w / w.sum()
+        dp = np.zeros_like(l)
+        for j, e in enumerate(sel):
+            dp[e] += dgate[j]
+        dl = p * (dp - float(p @ dp))
+    else:
+        s = sigmoid_f64(l[sel])
+        S = s.sum()
+        g = s / S
+        ds = (dgate - float(g @ dgate)) / S
+        dl[sel] = ds * s * (1.0 - s)
+    return dl
+
+
+def moe_backward(x, w_r, dy, k, E, R, mode, w13=None, w2=None,
+                 sel_bias=None, logit_offset=None, n_groups=1,
+                 topk_groups=1, group_score_topk=0, capacity=None,
+                 logits=None):
+    """Gradients of L = sum(dy * y) for the layer of moe_forward.
+
+    Returns dx [T, D], dw_r [E, D], dw13 [E, 2F, D], dw2 [E, D, F] (None for
+    identity experts), and the intermediates dgate [T, k] (0 for dropped
+    pairs), dlogits [T, E], dyp [N, D] (the gate-scaled upstream gradient in
+    the expert-contiguous order) and dxp [N, D] (the experts' input
+    gradients in that order)."""
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    T, D = x.shape
+    fw = moe_forward(x, w_r, k, E, R, mode, w13=w13, w2=w2,
+                     sel_bias=sel_bias, logit_offset=logit_offset,
+                     n_groups=n_groups, topk_groups=topk_groups,
+                     group_score_topk=group_score_topk, capacity=capacity,
+                     logits=logits)
+    idx, gate = fw["topk_idx"], fw["topk_gate"]
+    dst, off, src = fw["dst_row"], fw["offsets"], fw["src_pair"]
+    xp, yp = fw["xp"], fw["yp"]
+    N = len(src)
+    # dispatch of the upstream gradient: dyp[r] = g * dy[t]; dgate = dy . yp
+    dyp = np.zeros((N, D))
+    dgate = np.zeros((T, k))
+    for t in range(T):
+        for j in range(k):
+            r = int(dst[t * k + j])
+            if r >= 0:
+                dyp[r] = gate[t, j] * dy[t]
+                dgate[t, j] = float(dy[t] @ yp[r])
+    # experts
+    dxp = dyp.copy() if w13 is None else np.zeros((N, D))
+    dw13 = dw2 = None
+    if w13 is not None:
+        F = np.asarray(w13[0]).shape[0] // 2
+        dw13 = np.zeros((E, 2 * F, D))
+        dw2 = np.zeros((E, D, F))
+        for e in range(E):
+            a, b = int(off[e]), int(off[e + 1])
+            if b > a:
+                w1, w3 = split_w13(np.asarray(w13[e], dtype=np.float64))
+                dh, dw1, dw3, dw2e = expert_backward(xp[a:b], w1, w3, w2[e],
+                                                     dyp[a:b])
+                dxp[a:b] = dh
+                dw13[e, :F] = dw1
+                dw13[e, F:] = dw3
+                dw2[e] = dw2e
+    # combine of the input gradients: dx[t] = sum over kept j of dxp[row]
+    dx = np.zeros((T, D))
+    for t in range(T):
+        for j in range(k):
+            r = int(dst[t * k + j])
+            if r >= 0:
+                dx[t] += dxp[r]
+    # router
+    lg = fw["logits"] if "logits" in fw else logits
+    dlogits = np.zeros((T, E))
+    for t in range(T):
+        dlogits[t] = gate_backward(lg[t], idx[t], dgate[t], mode)
+    dw_r = dlogits.T @ x
+    dx += dlogits @ np.asarray(w_r, dtype=np.float64)
+    return dict(dx=dx, dw_r=dw_r, dw13=dw13, dw2=dw2, dgate=dgate,
+                dlogits=dlogits, dyp=dyp, dxp=dxp, forward=fw)
