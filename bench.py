@@ -496,6 +496,100 @@ def run_extras(args, local_rank, workload):
     return line
 
 
+# ------------------------------------------------------- training step
+def run_train(args, local_rank, workload):
+    """One training step of the layer: forward on the 64-row aligned layout
+    (forward_train) then the backward pass, timed with CUDA events per
+    stage, L2 flushed before every step.  The expert backward (five tcgen05
+    GEMMs) is reported against the sustained bf16 peak with its useful
+    FLOPs 16*N*D*F (dH 2, recomputed gate/up 4, dXp 4, dW2 2, dW13 4)."""
+    import torch
+    from combine_router_gemm_top_b300 import workloads as W
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = W.WORKLOADS[workload]
+    layer, inp = build_layer(wl, dev, wl.seed)
+    x = inp["x"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.seed + 17)
+    dy = torch.randn(x.shape, generator=g, device=dev).to(x.dtype)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    from combine_router_gemm_top_b300 import _lib as L
+    b = layer._train_buffers()
+    names = ["forward", "combine_bwd", "ffn_bwd", "permute_bwd", "route_bwd"]
+
+    def step(m=None):
+        rec = (lambda j: m[j].record(stream)) if m else (lambda j: None)
+        rec(0)
+        layer.forward_train(x, stream)
+        rec(1)
+        L.moe_combine_backward(wl.T, wl.k, wl.D, layer.dcode, dy, b["ya"],
+                               b["dst_a"], layer.topk_gate, b["dga"],
+                               b["dgate"], stream)
+        L.moe_aligned_fill(wl.E, wl.D, layer.dcode, layer.expert_offsets,
+                           b["off_a"], b["dga"], stream)
+        rec(2)
+        L.moe_grouped_ffn_backward(wl.E, wl.D, wl.F, b["rows"], layer.dcode,
+                                   b["xa"], b["dga"], b["off_a"], layer.w13,
+                                   layer.w2, b["dxa"], b["dw13"], b["dw2"],
+                                   b["bwd_ws"], layer.status, stream)
+        rec(3)
+        L.moe_permute_backward(wl.T, wl.k, wl.D, layer.dcode, b["dxa"],
+                               b["dst_a"], b["dx"], stream)
+        rec(4)
+        L.moe_route_backward(layer.cfg, x, layer.w_r, layer.logits,
+                             layer.topk_idx, b["dgate"], b["dlogits"],
+                             b["dw_r"], b["dx"], layer.status, stream)
+        rec(5)
+
+    layer._x = x
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    K = max(1, min(args.steps, 200))
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    marks = [[ev() for _ in range(6)] for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.5)
+    for i in range(K):
+        flush.zero_()
+        step(marks[i])
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if layer.device_status() != 0:
+        raise RuntimeError(f"device status {layer.device_status()}")
+    parts = {n: sum(m[j].elapsed_time(m[j + 1]) for m in marks) / K
+             for j, n in enumerate(names)}
+    total = sum(m[0].elapsed_time(m[5]) for m in marks) / K
+    peaks = load_peaks()
+    n_kept = int(layer.n_kept.item())
+    flops_bwd = 16.0 * n_kept * wl.D * wl.F
+    flops_fwd = 6.0 * n_kept * wl.D * wl.F
+    tf_bwd = flops_bwd / (parts["ffn_bwd"] / 1e3) / 1e12
+    line = {"mode": "train", "metric": "MoE-layer training-step tokens/s "
+                                       "(forward + backward) at 1 B300",
+            "value": round(wl.T / (total / 1e3), 1), "unit": "tokens/s",
+            "ms_per_step": round(total, 4), "steps": K,
+            "config": {"workload": wl.name, "T": wl.T, "D": wl.D, "E": wl.E,
+                       "k": wl.k, "F": wl.F, "n_kept": n_kept,
+                       "aligned_rows": int(b["off_a"][-1].item()),
+                       "l2": "flushed (256 MiB write) before every step"},
+            "per_stage_ms": {n: round(v, 4) for n, v in parts.items()},
+            "ffn_backward": {"tflops": round(tf_bwd, 1),
+                             "frac_of_sustained": round(
+                                 tf_bwd / peaks["bf16_tflops_sustained"], 4),
+                             "useful_flops": flops_bwd},
+            "forward_train_tflops": round(
+                flops_fwd / (parts["forward"] / 1e3) / 1e12, 1),
+            "clocks": clk}
+    del layer, inp, flush
+    torch.cuda.empty_cache()
+    return line
+
+
 # --------------------------------------------------------------- CPU oracle
 def oracle_sample_run(wl, inp, n_tok):
     """One pass of the CPU oracle (as it stands) over the first n_tok tokens
@@ -614,6 +708,9 @@ def main():
     ap.add_argument("--experts", type=int, default=0,
                     help="override the workload's expert count (small cases "
                          "for profiler captures)")
+    ap.add_argument("--train", action="store_true",
+                    help="time one training step (forward on the aligned "
+                         "layout + backward) of --workload")
     ap.add_argument("--extras", action="store_true",
                     help="time router statistics, the bias step, the "
                          "dispatch matrix and the padded static-capacity "
@@ -634,6 +731,11 @@ def main():
         from combine_router_gemm_top_b300 import build as B
         if rank == 0:
             B.build(verbose=False)
+        if args.train:
+            if rank == 0:
+                print(json.dumps(run_train(args, local_rank, args.workload)),
+                      flush=True)
+            return
         if args.extras:
             if rank == 0:
                 for name in ("switch_bf16", "deepseek_bf16", "mixtral_bf16",

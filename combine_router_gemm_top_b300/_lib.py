@@ -40,7 +40,10 @@ EXPORTED = ["moe_route_workspace_size", "moe_route",
             "moe_selftest_sigmoid_key", "moe_dispatch_layout_noalloc",
             "moe_router_stats_workspace_size", "moe_router_stats",
             "moe_router_bias_update", "moe_dispatch_matrix",
-            "moe_padded_layout", "moe_pad_fill",
+            "moe_padded_layout", "moe_pad_fill", "moe_aligned_layout",
+            "moe_aligned_fill", "moe_combine_backward",
+            "moe_permute_backward", "moe_grouped_ffn_backward_workspace_size",
+            "moe_grouped_ffn_backward", "moe_route_backward",
             "moe_status_str", "moe_abi_version"]
 ABI_VERSION = 1
 
@@ -91,6 +94,20 @@ _SIGS = {
     "moe_padded_layout": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp,
                                  _vp, _vp, _vp]),
     "moe_pad_fill": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp]),
+    "moe_aligned_layout": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp,
+                                  _vp, _vp, _vp, _vp]),
+    "moe_aligned_fill": (_i32, [_i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "moe_combine_backward": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp,
+                                    _vp, _vp, _vp, _vp]),
+    "moe_permute_backward": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp,
+                                    _vp]),
+    "moe_grouped_ffn_backward_workspace_size": (_sz, [_i32, _i32, _i32, _i32,
+                                                      _i32]),
+    "moe_grouped_ffn_backward": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp,
+                                        _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                        _vp, _sz, _vp, _vp]),
+    "moe_route_backward": (_i32, [ctypes.POINTER(RouteCfg), _vp, _vp, _vp,
+                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_selftest_bounded_wait": (_i32, [_vp, _u64, _vp]),
     "moe_selftest_sigmoid_key": (_i32, [_vp, _vp, _i32, _vp]),
     "moe_status_str": (ctypes.c_char_p, [_i32]),
@@ -271,6 +288,60 @@ def moe_padded_layout(T, k, E, capacity, topk_idx, dst_row, expert_offsets,
 def moe_pad_fill(E, capacity, D, dtype, expert_counts, buf, stream=None):
     _check(load().moe_pad_fill(E, capacity, D, dtype, _p(expert_counts),
                                _p(buf), _stream(stream)), "moe_pad_fill")
+
+
+def moe_aligned_layout(T, k, E, align, topk_idx, dst_row, expert_offsets,
+                       dst_row_aligned, offsets_aligned, status, stream=None):
+    _check(load().moe_aligned_layout(T, k, E, align, _p(topk_idx),
+                                     _p(dst_row), _p(expert_offsets),
+                                     _p(dst_row_aligned), _p(offsets_aligned),
+                                     _p(status), _stream(stream)),
+           "moe_aligned_layout")
+
+
+def moe_aligned_fill(E, D, dtype, expert_offsets, offsets_aligned, buf,
+                     stream=None):
+    _check(load().moe_aligned_fill(E, D, dtype, _p(expert_offsets),
+                                   _p(offsets_aligned), _p(buf),
+                                   _stream(stream)), "moe_aligned_fill")
+
+
+def moe_combine_backward(T, k, D, dtype, dy, yp, dst_row, topk_gate, dyp,
+                         dgate, stream=None):
+    _check(load().moe_combine_backward(T, k, D, dtype, _p(dy), _p(yp),
+                                       _p(dst_row), _p(topk_gate), _p(dyp),
+                                       _p(dgate), _stream(stream)),
+           "moe_combine_backward")
+
+
+def moe_permute_backward(T, k, D, dtype, dxp, dst_row, dx, stream=None):
+    _check(load().moe_permute_backward(T, k, D, dtype, _p(dxp), _p(dst_row),
+                                       _p(dx), _stream(stream)),
+           "moe_permute_backward")
+
+
+def moe_grouped_ffn_backward_workspace_size(E, D, F, max_rows, dtype) -> int:
+    return load().moe_grouped_ffn_backward_workspace_size(E, D, F, max_rows,
+                                                          dtype)
+
+
+def moe_grouped_ffn_backward(E, D, F, max_rows, dtype, xp, dyp,
+                             expert_offsets, w13, w2, dxp, dw13, dw2,
+                             workspace, status, stream=None):
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().moe_grouped_ffn_backward(
+        E, D, F, max_rows, dtype, _p(xp), _p(dyp), _p(expert_offsets),
+        _p(w13), _p(w2), _p(dxp), _p(dw13), _p(dw2), _p(workspace), nbytes,
+        _p(status), _stream(stream)), "moe_grouped_ffn_backward")
+
+
+def moe_route_backward(cfg, x, w_r, logits, topk_idx, dgate, dlogits, dw_r,
+                       dx, status, stream=None):
+    _check(load().moe_route_backward(ctypes.byref(cfg), _p(x), _p(w_r),
+                                     _p(logits), _p(topk_idx), _p(dgate),
+                                     _p(dlogits), _p(dw_r), _p(dx),
+                                     _p(status), _stream(stream)),
+           "moe_route_backward")
 
 
 def moe_selftest_bounded_wait(status, limit_ns, stream=None):

@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmoe.so")
 SOURCES = ["api.cu", "route.cu", "layout.cu", "permute_combine.cu",
            "grouped_ffn.cu", "layout_noalloc.cu", "router_stats.cu",
-           "dispatch_extras.cu"]
+           "dispatch_extras.cu", "backward.cu"]
 HEADERS = ["common.cuh", "ptx.cuh", "umma_gemm.cuh", "internal.h"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

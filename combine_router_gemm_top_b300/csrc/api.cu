@@ -323,6 +323,128 @@ moe_status moe_pad_fill(int32_t E, int32_t capacity, int32_t D, int32_t dtype,
                          reinterpret_cast<cudaStream_t>(stream), num_sms());
 }
 
+moe_status moe_aligned_layout(int32_t T, int32_t k, int32_t E, int32_t align,
+                              const int32_t* topk_idx, const int32_t* dst_row,
+                              const int32_t* expert_offsets,
+                              int32_t* dst_row_aligned,
+                              int32_t* offsets_aligned, int32_t* status,
+                              moe_stream_t stream) {
+  if (T < 0 || k < 1 || k > 32 || E < 1 || E > kLayoutMaxE || align < 1 ||
+      align > 1024)
+    return MOE_ERR_INVALID;
+  if (static_cast<int64_t>(T) * k + static_cast<int64_t>(align - 1) * E >
+      INT32_MAX)
+    return MOE_ERR_INVALID;
+  if (expert_offsets == nullptr || offsets_aligned == nullptr)
+    return MOE_ERR_INVALID;
+  if (T > 0 && (topk_idx == nullptr || dst_row == nullptr ||
+                dst_row_aligned == nullptr))
+    return MOE_ERR_INVALID;
+  return launch_aligned_layout(T, k, E, align, topk_idx, dst_row,
+                               expert_offsets, dst_row_aligned,
+                               offsets_aligned, status,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_aligned_fill(int32_t E, int32_t D, int32_t dtype,
+                            const int32_t* expert_offsets,
+                            const int32_t* offsets_aligned, void* buf,
+                            moe_stream_t stream) {
+  if (E < 1 || !rows_ok(1, 1, D, dtype)) return MOE_ERR_INVALID;
+  if (expert_offsets == nullptr || offsets_aligned == nullptr ||
+      buf == nullptr || !aligned(buf, 16))
+    return MOE_ERR_INVALID;
+  return launch_aligned_fill(E, D, dtype, expert_offsets, offsets_aligned,
+                             buf, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_combine_backward(int32_t T, int32_t k, int32_t D, int32_t dtype,
+                                const void* dy, const void* yp,
+                                const int32_t* dst_row, const float* topk_gate,
+                                void* dyp, float* dgate, moe_stream_t stream) {
+  if (!rows_ok(T, k, D, dtype)) return MOE_ERR_INVALID;
+  if (T == 0) return MOE_OK;
+  if (dy == nullptr || yp == nullptr || dst_row == nullptr ||
+      topk_gate == nullptr || dyp == nullptr || dgate == nullptr)
+    return MOE_ERR_INVALID;
+  if (!aligned(dy, 16) || !aligned(yp, 16) || !aligned(dyp, 16))
+    return MOE_ERR_INVALID;
+  return launch_combine_backward(T, k, D, dtype, dy, yp, dst_row, topk_gate,
+                                 dyp, dgate,
+                                 reinterpret_cast<cudaStream_t>(stream),
+                                 num_sms());
+}
+
+moe_status moe_permute_backward(int32_t T, int32_t k, int32_t D, int32_t dtype,
+                                const void* dxp, const int32_t* dst_row,
+                                void* dx, moe_stream_t stream) {
+  if (!rows_ok(T, k, D, dtype)) return MOE_ERR_INVALID;
+  if (T == 0) return MOE_OK;
+  if (dxp == nullptr || dst_row == nullptr || dx == nullptr)
+    return MOE_ERR_INVALID;
+  if (!aligned(dxp, 16) || !aligned(dx, 16)) return MOE_ERR_INVALID;
+  return launch_combine(T, k, D, dtype, dxp, dst_row, nullptr, dx,
+                        reinterpret_cast<cudaStream_t>(stream), num_sms());
+}
+
+size_t moe_grouped_ffn_backward_workspace_size(int32_t E, int32_t D, int32_t F,
+                                               int32_t max_rows,
+                                               int32_t dtype) {
+  if (E < 1 || D <= 0 || F <= 0 || max_rows < 0 || dtype != MOE_BF16)
+    return 0;
+  const size_t b = ffn_bwd_ws_bytes(F, max_rows);
+  return b > 0 ? b : 16;
+}
+
+moe_status moe_grouped_ffn_backward(
+    int32_t E, int32_t D, int32_t F, int32_t max_rows, int32_t dtype,
+    const void* xp, const void* dyp, const int32_t* expert_offsets,
+    const void* w13, const void* w2, void* dxp, float* dw13, float* dw2,
+    void* workspace, size_t workspace_bytes, int32_t* status,
+    moe_stream_t stream) {
+  if (E < 1 || D <= 0 || F <= 0 || max_rows < 0 || !valid_dtype(dtype))
+    return MOE_ERR_INVALID;
+  if (dtype != MOE_BF16 || D % 128 != 0 || F % 128 != 0 ||
+      E > kMaxGroupsApi)
+    return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(E) * 2 * F > INT32_MAX ||
+      static_cast<int64_t>(E) * D > INT32_MAX)
+    return MOE_ERR_UNSUPPORTED;
+  if (xp == nullptr || dyp == nullptr || expert_offsets == nullptr ||
+      w13 == nullptr || w2 == nullptr || dxp == nullptr || dw13 == nullptr ||
+      dw2 == nullptr || workspace == nullptr)
+    return MOE_ERR_INVALID;
+  if (!aligned(xp, 256) || !aligned(dyp, 256) || !aligned(w13, 256) ||
+      !aligned(w2, 256) || !aligned(workspace, 256) || !aligned(dxp, 16) ||
+      !aligned(dw13, 16) || !aligned(dw2, 16))
+    return MOE_ERR_INVALID;
+  if (workspace_bytes < ffn_bwd_ws_bytes(F, max_rows)) return MOE_ERR_INVALID;
+  return launch_grouped_ffn_backward(E, D, F, max_rows, xp, dyp,
+                                     expert_offsets, w13, w2, dxp, dw13, dw2,
+                                     workspace, status,
+                                     reinterpret_cast<cudaStream_t>(stream),
+                                     num_sms());
+}
+
+moe_status moe_route_backward(const moe_route_cfg* cfg, const void* x,
+                              const void* w_r, const float* logits,
+                              const int32_t* topk_idx, const float* dgate,
+                              float* dlogits, float* dw_r, void* dx,
+                              int32_t* status, moe_stream_t stream) {
+  (void)status;
+  if (!route_cfg_ok(cfg)) return MOE_ERR_INVALID;
+  if (cfg->T == 0) return MOE_OK;
+  if (logits == nullptr || topk_idx == nullptr || dgate == nullptr ||
+      dlogits == nullptr)
+    return MOE_ERR_INVALID;
+  if (dw_r != nullptr && x == nullptr) return MOE_ERR_INVALID;
+  if (dx != nullptr && w_r == nullptr) return MOE_ERR_INVALID;
+  return launch_route_backward(cfg->T, cfg->D, cfg->E, cfg->k, cfg->score,
+                               cfg->dtype, x, w_r, logits, topk_idx, dgate,
+                               dlogits, dw_r, dx,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
 moe_status moe_selftest_bounded_wait(int32_t* status, uint64_t limit_ns,
                                      moe_stream_t stream) {
   if (status == nullptr) return MOE_ERR_INVALID;

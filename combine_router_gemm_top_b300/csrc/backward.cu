@@ -1,0 +1,417 @@
+// Backward pass of the MoE layer, the row movers and the router
+// ("Expert Parallelism in LLMs", Backward Pass Symmetry: the upstream
+// gradient dL/dy goes to the experts along the dispatch pattern, the input
+// gradients return along the combine pattern).  The routing decision is
+// held fixed; gradients flow through the gates and the experts.
+//
+//   combine backward  dYp[row(t,j)] = g[t,j] * dy[t] and
+//                     dgate[t,j] = dy[t] . Yp[row(t,j)] (fp32, 0 if dropped)
+//   permute backward  dx[t] = sum over kept j of dXp[row(t,j)] (the combine
+//                     kernel with unit gates)
+//   aligned layout    expert segments moved to 64-row boundaries so that the
+//                     weight-gradient GEMMs, which contract over an expert's
+//                     token rows, never reach into the next expert; padding
+//                     rows are zero
+//   router backward   dlogits from dgate per score mode, dW_r = dlogits^T x,
+//                     dx += dlogits W_r (fp32 accumulation, fixed order)
+#include <float.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int kBwdWarps = 8;
+
+__device__ __forceinline__ float bwd_warp_sum(float v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
+}
+
+// ------------------------------------------------------ combine backward
+// One warp per token.  For each kept slot: the gate-scaled copy of dy[t]
+// into the slot's expert row and the dot product of dy[t] with the expert
+// output row.  dy[t] is re-read per slot from L1/L2.
+template <typename T>
+__global__ void __launch_bounds__(kBwdWarps * 32)
+    combine_backward_kernel(int64_t n_tok, int k, int nvec,
+                            const uint4* __restrict__ dy,
+                            const uint4* __restrict__ yp,
+                            const int32_t* __restrict__ dst_row,
+                            const float* __restrict__ gate,
+                            uint4* __restrict__ dyp,
+                            float* __restrict__ dgate) {
+  constexpr int N = Vec16<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kBwdWarps + (threadIdx.x >> 5);
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kBwdWarps;
+  for (int64_t t = w0; t < n_tok; t += nw) {
+    const int32_t my_dst = lane < k ? __ldg(dst_row + t * k + lane) : -1;
+    const float my_g = lane < k ? __ldg(gate + t * k + lane) : 0.0f;
+    const uint4* src = dy + t * nvec;
+    float my_dot = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const int32_t r = __shfl_sync(0xffffffffu, my_dst, j);
+      const float g = __shfl_sync(0xffffffffu, my_g, j);
+      if (r < 0) continue;
+      const uint4* yrow = yp + static_cast<int64_t>(r) * nvec;
+      uint4* drow = dyp + static_cast<int64_t>(r) * nvec;
+      float dot = 0.0f;
+      for (int v = lane; v < nvec; v += 32) {
+        float a[N], b[N], o[N];
+        Vec16<T>::to_f32(ld_nc_v4(src + v), a);
+        Vec16<T>::to_f32(ld_nc_v4(yrow + v), b);
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+          dot = fmaf(a[i], b[i], dot);
+          o[i] = g * a[i];
+        }
+        st_v4(drow + v, Vec16<T>::from_f32(o));
+      }
+      dot = bwd_warp_sum(dot);
+      if (lane == j) my_dot = dot;
+    }
+    if (lane < k) dgate[t * k + lane] = my_dst >= 0 ? my_dot : 0.0f;
+  }
+}
+
+moe_status launch_combine_backward(int T, int k, int D, int dtype,
+                                   const void* dy, const void* yp,
+                                   const int32_t* dst_row, const float* gate,
+                                   void* dyp, float* dgate,
+                                   cudaStream_t stream, int num_sms) {
+  if (T == 0) return MOE_OK;
+  const int nvec = static_cast<int>(D * dtype_bytes(dtype) / 16);
+  const int64_t want = ceil_div(T, kBwdWarps);
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+  if (dtype == MOE_BF16)
+    combine_backward_kernel<__nv_bfloat16><<<grid, kBwdWarps * 32, 0, stream>>>(
+        T, k, nvec, static_cast<const uint4*>(dy),
+        static_cast<const uint4*>(yp), dst_row, gate,
+        static_cast<uint4*>(dyp), dgate);
+  else
+    combine_backward_kernel<float><<<grid, kBwdWarps * 32, 0, stream>>>(
+        T, k, nvec, static_cast<const uint4*>(dy),
+        static_cast<const uint4*>(yp), dst_row, gate,
+        static_cast<uint4*>(dyp), dgate);
+  return launch_status();
+}
+
+// ------------------------------------------------------ aligned layout
+// One block: offsets_aligned = exclusive scan of round_up(count_e, align).
+__global__ void __launch_bounds__(1024)
+    aligned_offsets_kernel(int E, int align, const int32_t* __restrict__ off,
+                           int32_t* __restrict__ off_a) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t carry;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < E; base += 1024) {
+    const int e = base + threadIdx.x;
+    int v = 0;
+    if (e < E) {
+      const int c = __ldg(off + e + 1) - __ldg(off + e);
+      v = (c + align - 1) / align * align;
+    }
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += u;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_tot[lane];
+      int wi = w;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, wi, d);
+        if (lane >= d) wi += u;
+      }
+      warp_tot[lane] = wi - w;   // exclusive prefix of warp totals
+    }
+    __syncthreads();
+    const int c0 = carry;
+    if (e < E) off_a[e] = c0 + warp_tot[warp] + incl - v;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = c0 + warp_tot[31] + incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) off_a[E] = carry;
+}
+
+__global__ void aligned_rows_kernel(int64_t P, int E,
+                                    const int32_t* __restrict__ topk_idx,
+                                    const int32_t* __restrict__ dst_row,
+                                    const int32_t* __restrict__ off,
+                                    const int32_t* __restrict__ off_a,
+                                    int32_t* __restrict__ dst_a,
+                                    int32_t* status) {
+  const int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (p >= P) return;
+  const int r = __ldg(dst_row + p);
+  int out = -1;
+  if (r >= 0) {
+    const int e = __ldg(topk_idx + p);
+    if (e >= 0 && e < E)
+      out = __ldg(off_a + e) + (r - __ldg(off + e));
+    else
+      set_status(status, MOE_ERR_INDEX);
+  }
+  dst_a[p] = out;
+}
+
+moe_status launch_aligned_layout(int T, int k, int E, int align,
+                                 const int32_t* topk_idx,
+                                 const int32_t* dst_row,
+                                 const int32_t* offsets,
+                                 int32_t* dst_row_aligned,
+                                 int32_t* offsets_aligned, int32_t* status,
+                                 cudaStream_t stream) {
+  aligned_offsets_kernel<<<1, 1024, 0, stream>>>(E, align, offsets,
+                                                 offsets_aligned);
+  const int64_t P = static_cast<int64_t>(T) * k;
+  if (P > 0)
+    aligned_rows_kernel<<<static_cast<unsigned>(ceil_div(P, 256)), 256, 0,
+                          stream>>>(P, E, topk_idx, dst_row, offsets,
+                                    offsets_aligned, dst_row_aligned, status);
+  return launch_status();
+}
+
+// Zero rows [off_a[e] + count_e, off_a[e+1]) of every expert: one block per
+// expert, one warp per padding row.
+__global__ void __launch_bounds__(256)
+    aligned_fill_kernel(int nvec, const int32_t* __restrict__ off,
+                        const int32_t* __restrict__ off_a,
+                        uint4* __restrict__ buf) {
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int r0 = __ldg(off_a + e) + (__ldg(off + e + 1) - __ldg(off + e));
+  const int r1 = __ldg(off_a + e + 1);
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int r = r0 + (threadIdx.x >> 5); r < r1; r += 8) {
+    uint4* row = buf + static_cast<int64_t>(r) * nvec;
+    for (int v = lane; v < nvec; v += 32) st_v4(row + v, z);
+  }
+}
+
+moe_status launch_aligned_fill(int E, int D, int dtype, const int32_t* offsets,
+                               const int32_t* offsets_aligned, void* buf,
+                               cudaStream_t stream) {
+  const int nvec = static_cast<int>(D * dtype_bytes(dtype) / 16);
+  aligned_fill_kernel<<<static_cast<unsigned>(E), 256, 0, stream>>>(
+      nvec, offsets, offsets_aligned, static_cast<uint4*>(buf));
+  return launch_status();
+}
+
+// ------------------------------------------------------ router backward
+// One warp per token; lane l holds experts l + 32 i.  Slot j's id, gate
+// gradient and logit live in lane j (k <= 32).
+template <int NI>
+__global__ void __launch_bounds__(kBwdWarps * 32)
+    dlogits_kernel(int T, int E, int k, int score,
+                   const float* __restrict__ logits,
+                   const int32_t* __restrict__ topk_idx,
+                   const float* __restrict__ dgate,
+                   float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kBwdWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const bool slot = lane < k;
+  const int my_e = slot ? topk_idx[t * k + lane] : -1;
+  const float my_dg = slot ? dgate[t * k + lane] : 0.0f;
+  const bool my_ok = slot && my_e >= 0 && my_e < E;
+  const float my_l = my_ok ? logits[t * E + my_e] : 0.0f;
+  float out[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) out[i] = 0.0f;
+
+  if (score == MOE_SCORE_SOFTMAX_FULL) {
+    // g_j = p_{e_j}, p = softmax over all E: dl = p (dp - p . dp)
+    float l[NI], p[NI], dp[NI];
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int e = lane + 32 * i;
+      l[i] = e < E ? logits[t * E + e] : -FLT_MAX;
+      m = fmaxf(m, l[i]);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1)
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    float z = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      p[i] = lane + 32 * i < E ? expf(l[i] - m) : 0.0f;
+      z += p[i];
+      dp[i] = 0.0f;
+    }
+    z = bwd_warp_sum(z);
+    for (int j = 0; j < k; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, my_ok ? my_e : -1, j);
+      const float gj = __shfl_sync(0xffffffffu, my_dg, j);
+#pragma unroll
+      for (int i = 0; i < NI; ++i)
+        if (lane + 32 * i == ej) dp[i] += gj;
+    }
+    float pdp = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      p[i] = p[i] / z;
+      pdp += p[i] * dp[i];
+    }
+    pdp = bwd_warp_sum(pdp);
+#pragma unroll
+    for (int i = 0; i < NI; ++i) out[i] = p[i] * (dp[i] - pdp);
+  } else {
+    float dl_slot = 0.0f;
+    if (score == MOE_SCORE_SOFTMAX_TOPK) {
+      // g = softmax over the selected logits: dl_j = g_j (dg_j - g . dg)
+      float m = my_ok ? my_l : -FLT_MAX;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+      const float ex = my_ok ? expf(my_l - m) : 0.0f;
+      const float g = ex / bwd_warp_sum(ex);
+      const float gdg = bwd_warp_sum(g * my_dg);
+      dl_slot = g * (my_dg - gdg);
+    } else {
+      // g_j = s_j / S over the selected sigmoid scores:
+      // dl_j = (dg_j - g . dg) / S * s_j (1 - s_j)
+      const float s = my_ok ? 1.0f / (1.0f + expf(-my_l)) : 0.0f;
+      const float S = bwd_warp_sum(s);
+      const float g = s / S;
+      const float gdg = bwd_warp_sum(g * my_dg);
+      dl_slot = (my_dg - gdg) / S * s * (1.0f - s);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, my_ok ? my_e : -1, j);
+      const float dj = __shfl_sync(0xffffffffu, dl_slot, j);
+#pragma unroll
+      for (int i = 0; i < NI; ++i)
+        if (lane + 32 * i == ej) out[i] += dj;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) dlogits[t * E + e] = out[i];
+  }
+}
+
+// dW_r[e, d] = sum_t dl[t, e] x[t, d]: block (256 d, 8 experts), tokens in
+// a fixed order.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    dwr_kernel(int Tn, int E, int D, const float* __restrict__ dl,
+               const T* __restrict__ x, float* __restrict__ dwr) {
+  __shared__ float s_dl[64][8];
+  const int d = blockIdx.x * 256 + threadIdx.x;
+  const int e0 = blockIdx.y * 8;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int t0 = 0; t0 < Tn; t0 += 64) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
+      const int tt = t0 + i / 8, ee = e0 + i % 8;
+      s_dl[i / 8][i % 8] = tt < Tn && ee < E ? dl[static_cast<int64_t>(tt) * E + ee] : 0.0f;
+    }
+    __syncthreads();
+    if (d < D) {
+      const int tn = min(64, Tn - t0);
+      for (int i = 0; i < tn; ++i) {
+        const float xv = static_cast<float>(x[static_cast<int64_t>(t0 + i) * D + d]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(s_dl[i][j], xv, acc[j]);
+      }
+    }
+  }
+  if (d < D) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (e0 + j < E) dwr[static_cast<int64_t>(e0 + j) * D + d] = acc[j];
+  }
+}
+
+// dx[t, d] += sum_e dl[t, e] W_r[e, d]: block (256 d, 8 tokens).
+template <typename T>
+__global__ void __launch_bounds__(256)
+    dx_router_kernel(int Tn, int E, int D, const float* __restrict__ dl,
+                     const T* __restrict__ wr, T* __restrict__ dx) {
+  extern __shared__ float s_dlt[];   // [8][E]
+  const int d = blockIdx.x * 256 + threadIdx.x;
+  const int t0 = blockIdx.y * 8;
+  for (int i = threadIdx.x; i < 8 * E; i += 256) {
+    const int tt = t0 + i / E;
+    s_dlt[i] = tt < Tn ? dl[static_cast<int64_t>(tt) * E + i % E] : 0.0f;
+  }
+  __syncthreads();
+  if (d >= D) return;
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  for (int e = 0; e < E; ++e) {
+    const float w = static_cast<float>(wr[static_cast<int64_t>(e) * D + d]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = fmaf(s_dlt[j * E + e], w, acc[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int tt = t0 + j;
+    if (tt < Tn) {
+      T* p = dx + static_cast<int64_t>(tt) * D + d;
+      *p = static_cast<T>(static_cast<float>(*p) + acc[j]);
+    }
+  }
+}
+
+moe_status launch_route_backward(int T, int D, int E, int k, int score,
+                                 int dtype, const void* x, const void* w_r,
+                                 const float* logits, const int32_t* topk_idx,
+                                 const float* dgate, float* dlogits,
+                                 float* dw_r, void* dx, cudaStream_t stream) {
+  if (T == 0) {
+    return MOE_OK;
+  }
+  const unsigned g1 = static_cast<unsigned>(ceil_div(T, kBwdWarps));
+  const int ni = static_cast<int>(ceil_div(E, 32));
+  if (ni <= 1)
+    dlogits_kernel<1><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits);
+  else if (ni <= 2)
+    dlogits_kernel<2><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits);
+  else if (ni <= 4)
+    dlogits_kernel<4><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits);
+  else
+    dlogits_kernel<8><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits);
+  const dim3 gw(static_cast<unsigned>(ceil_div(D, 256)),
+                static_cast<unsigned>(ceil_div(E, 8)));
+  const dim3 gx(static_cast<unsigned>(ceil_div(D, 256)),
+                static_cast<unsigned>(ceil_div(T, 8)));
+  const size_t smem = static_cast<size_t>(8) * E * sizeof(float);
+  if (dtype == MOE_BF16) {
+    if (dw_r != nullptr)
+      dwr_kernel<__nv_bfloat16><<<gw, 256, 0, stream>>>(
+          T, E, D, dlogits, static_cast<const __nv_bfloat16*>(x), dw_r);
+    if (dx != nullptr)
+      dx_router_kernel<__nv_bfloat16><<<gx, 256, smem, stream>>>(
+          T, E, D, dlogits, static_cast<const __nv_bfloat16*>(w_r),
+          static_cast<__nv_bfloat16*>(dx));
+  } else {
+    if (dw_r != nullptr)
+      dwr_kernel<float><<<gw, 256, 0, stream>>>(
+          T, E, D, dlogits, static_cast<const float*>(x), dw_r);
+    if (dx != nullptr)
+      dx_router_kernel<float><<<gx, 256, smem, stream>>>(
+          T, E, D, dlogits, static_cast<const float*>(w_r),
+          static_cast<float*>(dx));
+  }
+  return launch_status();
+}
+
+}  // namespace moe

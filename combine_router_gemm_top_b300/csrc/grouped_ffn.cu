@@ -177,3 +177,113 @@ moe_status launch_selftest_wait(int32_t* status, uint64_t limit_ns,
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// ----------------------------------------------------------- backward
+// Workspace of the backward: dH [rows, F], dGU [rows, 2F], H [rows, F]
+// (bf16 each).
+size_t ffn_bwd_ws_bytes(int F, int max_rows) {
+  return static_cast<size_t>(max_rows) * F * 2 * 4;
+}
+
+moe_status launch_grouped_ffn_backward(int E, int D, int F, int max_rows,
+                                       const void* xp, const void* dyp,
+                                       const int32_t* offsets,
+                                       const void* w13, const void* w2,
+                                       void* dxp, float* dw13, float* dw2,
+                                       void* ws, int32_t* status,
+                                       cudaStream_t stream, int num_sms) {
+  if (max_rows == 0) return MOE_OK;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const size_t rf = static_cast<size_t>(max_rows) * F * 2;
+  void* dh = w;
+  void* dgu = w + rf;
+  void* h = w + 3 * rf;
+  const int64_t EF2 = static_cast<int64_t>(E) * 2 * F;
+  const int64_t ED = static_cast<int64_t>(E) * D;
+  CUtensorMap t_dyp, t_w2mn, t_xp, t_w13, t_dgu, t_w13mn, t_dyp_mn, t_h_mn,
+      t_dgu_mn, t_xp_mn;
+  if (!make_tmap_bf16_2d(&t_dyp, dyp, D, max_rows, kBM) ||
+      !make_tmap_bf16_2d(&t_w2mn, w2, F, ED, 64) ||
+      !make_tmap_bf16_2d(&t_xp, xp, D, max_rows, kBM) ||
+      !make_tmap_bf16_2d(&t_w13, w13, D, EF2, 128) ||
+      !make_tmap_bf16_2d(&t_dgu, dgu, 2 * F, max_rows, kBM) ||
+      !make_tmap_bf16_2d(&t_w13mn, w13, D, EF2, 64) ||
+      !make_tmap_bf16_2d(&t_dyp_mn, dyp, D, max_rows, 64) ||
+      !make_tmap_bf16_2d(&t_h_mn, h, F, max_rows, 64) ||
+      !make_tmap_bf16_2d(&t_dgu_mn, dgu, 2 * F, max_rows, 64) ||
+      !make_tmap_bf16_2d(&t_xp_mn, xp, D, max_rows, 64))
+    return MOE_ERR_CUDA;
+
+  GemmArgs base{};
+  base.M = max_rows;
+  base.BN = 256;
+  base.stages = 4;
+  base.tmem_cols = 512;
+  base.groups = E;
+  base.F = F;
+  base.offsets = offsets;
+  base.status = status;
+  base.wait_limit_ns = kWaitLimitNs;
+
+  // dH = dYp . W2_e   (B = W2 [D, F] read MN-major)
+  GemmArgs g = base;
+  g.k_blocks = D / kBK;
+  g.n_tiles = static_cast<int>(ceil_div(F, 256));
+  g.b_rows_per_group = D;
+  g.out = dh;
+  g.out_ld = F;
+  g.out_cols = F;
+  moe_status s = launch_umma<kDH>(t_dyp, t_w2mn, g, stream, num_sms);
+  if (s != MOE_OK) return s;
+
+  // recompute gate/up, then dG, dU (into dGU) and H
+  g = base;
+  g.k_blocks = D / kBK;
+  g.n_tiles = F / 128;
+  g.b_rows_per_group = 2 * F;
+  g.aux_in = dh;
+  g.out = dgu;
+  g.out2 = h;
+  g.out_ld = F;
+  g.out_cols = F;
+  s = launch_umma<kUpBwd>(t_xp, t_w13, g, stream, num_sms);
+  if (s != MOE_OK) return s;
+
+  // dXp = dGU . W13_e   (B = W13 [2F, D] read MN-major)
+  g = base;
+  g.k_blocks = 2 * F / kBK;
+  g.n_tiles = static_cast<int>(ceil_div(D, 256));
+  g.b_rows_per_group = 2 * F;
+  g.out = dxp;
+  g.out_ld = D;
+  g.out_cols = D;
+  s = launch_umma<kDX>(t_dgu, t_w13mn, g, stream, num_sms);
+  if (s != MOE_OK) return s;
+
+  // dW2_e = dYp_e^T . H_e   [D, F] per expert, fp32
+  g = base;
+  g.m_total = D;
+  g.m_tiles = D / kBM;
+  g.n_tiles = static_cast<int>(ceil_div(F, 256));
+  g.M = static_cast<int32_t>(ED);
+  g.out = dw2;
+  g.out_ld = F;
+  g.out_cols = F;
+  s = launch_umma<kWG2>(t_dyp_mn, t_h_mn, g, stream, num_sms);
+  if (s != MOE_OK) return s;
+
+  // dW13_e = dGU_e^T . Xp_e   [2F, D] per expert, fp32
+  g = base;
+  g.m_total = 2 * F;
+  g.m_tiles = 2 * F / kBM;
+  g.n_tiles = static_cast<int>(ceil_div(D, 256));
+  g.M = static_cast<int32_t>(EF2);
+  g.out = dw13;
+  g.out_ld = D;
+  g.out_cols = D;
+  return launch_umma<kWG13>(t_dgu_mn, t_xp_mn, g, stream, num_sms);
+}
+
+}  // namespace moe

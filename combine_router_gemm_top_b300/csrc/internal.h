@@ -96,6 +96,35 @@ moe_status launch_pad_fill(int E, int capacity, int D, int dtype,
                            const int32_t* counts, void* buf,
                            cudaStream_t stream, int num_sms);
 
+size_t ffn_bwd_ws_bytes(int F, int max_rows);
+moe_status launch_grouped_ffn_backward(int E, int D, int F, int max_rows,
+                                       const void* xp, const void* dyp,
+                                       const int32_t* offsets,
+                                       const void* w13, const void* w2,
+                                       void* dxp, float* dw13, float* dw2,
+                                       void* ws, int32_t* status,
+                                       cudaStream_t stream, int num_sms);
+moe_status launch_combine_backward(int T, int k, int D, int dtype,
+                                   const void* dy, const void* yp,
+                                   const int32_t* dst_row, const float* gate,
+                                   void* dyp, float* dgate,
+                                   cudaStream_t stream, int num_sms);
+moe_status launch_aligned_layout(int T, int k, int E, int align,
+                                 const int32_t* topk_idx,
+                                 const int32_t* dst_row,
+                                 const int32_t* offsets,
+                                 int32_t* dst_row_aligned,
+                                 int32_t* offsets_aligned, int32_t* status,
+                                 cudaStream_t stream);
+moe_status launch_aligned_fill(int E, int D, int dtype, const int32_t* offsets,
+                               const int32_t* offsets_aligned, void* buf,
+                               cudaStream_t stream);
+moe_status launch_route_backward(int T, int D, int E, int k, int score,
+                                 int dtype, const void* x, const void* w_r,
+                                 const float* logits, const int32_t* topk_idx,
+                                 const float* dgate, float* dlogits,
+                                 float* dw_r, void* dx, cudaStream_t stream);
+
 moe_status launch_sigmoid_key(const float* l, float* out, int n,
                               cudaStream_t stream);
 moe_status launch_selftest_wait(int32_t* status, uint64_t limit_ns,

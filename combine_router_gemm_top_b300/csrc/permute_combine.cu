@@ -64,7 +64,10 @@ __global__ void __launch_bounds__(kRowWarps * 32)
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kRowWarps;
   for (int64_t t = warp_g; t < n_tok; t += nwarps) {
     const int32_t my_dst = lane < k ? __ldg(dst_row + t * k + lane) : -1;
-    const float my_g = lane < k ? __ldg(gate + t * k + lane) : 0.0f;
+    // gate == nullptr: unit gates (the permute backward sums the rows)
+    const float my_g =
+        lane < k ? (gate != nullptr ? __ldg(gate + t * k + lane) : 1.0f)
+                 : 0.0f;
     uint4* out = y + t * nvec;
     for (int v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
       float acc[kUnroll][N];

@@ -134,6 +134,22 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory descriptor for an MN-major operand tile built from TMA
+// boxes of 64 MN elements (128 bytes, the contiguous dimension) by 64 K
+// rows with the 128-byte swizzle: K rows are 128 bytes apart, 8-row K
+// groups 1024 bytes apart (stride byte offset), and each further 64-element
+// MN block is the next 8 KB box (leading byte offset).  Stepping K by 16
+// rows adds 2048 bytes (128 in the >>4 address field).
+__device__ __forceinline__ uint64_t umma_desc_mn_sw128(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(8192 >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32
 // accumulator, both operands K-major, shape M x N (x 16).  Fields: D format
 // (bits 4-5, 1 = f32), A format (7-9, 1 = bf16), B format (10-12, 1 =
@@ -142,6 +158,14 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) |
          (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same with either operand MN-major (bit 15: A, bit 16: B).
+__host__ __device__ constexpr uint32_t umma_idesc_bf16_major(int M, int N,
+                                                             bool a_mn,
+                                                             bool b_mn) {
+  return umma_idesc_bf16(M, N) | (a_mn ? (1u << 15) : 0u) |
+         (b_mn ? (1u << 16) : 0u);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one 128 x N x 16 step, issued by one

@@ -24,6 +24,20 @@
 //           H = SiLU(gate) * up rounded to bf16.
 //   kDown   grouped down-projection: B = 256 rows of W2, epilogue rounds to
 //           bf16.
+// Backward modes (training path; expert segments start on 64-row
+// boundaries and padding rows are zero):
+//   kDH     dH = dYp . W2_e: A = dYp rows (K = D, K-major), B = W2 [D, F]
+//           read MN-major (F contiguous); bf16 out [rows, F].
+//   kUpBwd  recomputes gate and up as kUp does; the epilogue reads dH and
+//           writes dG = dH * up * SiLU'(gate) and dU = dH * SiLU(gate) into
+//           dGU [rows, 2F] (W13's row order) and H = SiLU(gate) * up.
+//   kDX     dXp = dGU . W13_e: A = dGU rows (K = 2F), B = W13 [2F, D] read
+//           MN-major; bf16 out [rows, D].
+//   kWG2    dW2_e = dYp_e^T . H_e and
+//   kWG13   dW13_e = dGU_e^T . Xp_e: both operands MN-major over the
+//           expert's token rows (the contraction), tile = (expert, 128
+//           output rows, 256 output columns), fp32 out.  An expert with no
+//           rows gets zeros.
 // Ragged tails (grouped modes): the last row block of an expert with at most
 // 112 rows runs with the operands swapped.  The same shared-memory tiles
 // feed two MMAs of shape 128 x n x 16, n = the tail rounded up to 16: the
@@ -45,7 +59,26 @@
 
 namespace moe {
 
-enum GemmMode { kRoute = 0, kUp = 1, kDown = 2 };
+enum GemmMode {
+  kRoute = 0, kUp = 1, kDown = 2,
+  kDH = 3, kUpBwd = 4, kDX = 5, kWG2 = 6, kWG13 = 7
+};
+
+// Static properties of a mode.
+template <int MODE>
+struct ModeInfo {
+  // token rows on M, ragged per expert (tiles from the expert offsets)
+  static constexpr bool grouped_m = MODE == kUp || MODE == kDown ||
+                                    MODE == kDH || MODE == kUpBwd ||
+                                    MODE == kDX;
+  // per-expert weight gradient: M x N output, K = the expert's token rows
+  static constexpr bool wgrad = MODE == kWG2 || MODE == kWG13;
+  static constexpr bool a_mn = wgrad;
+  static constexpr bool b_mn = MODE == kDH || MODE == kDX || wgrad;
+  static constexpr bool swap_tails = MODE == kUp || MODE == kDown;
+  // B tile is gate rows stacked on up rows
+  static constexpr bool gate_up = MODE == kUp || MODE == kUpBwd;
+};
 
 constexpr int kBM = 128;          // tile rows (TMEM lanes)
 constexpr int kBK = 64;           // K elements per stage (one 128-byte row)
@@ -75,6 +108,11 @@ struct GemmArgs {
   int32_t out_cols;         // valid output columns
   int32_t* status;
   uint64_t wait_limit_ns;
+  // backward modes
+  const void* aux_in;       // kUpBwd: dH [rows, F]
+  void* out2;               // kUpBwd: H [rows, F]
+  int32_t m_total;          // wgrad: output rows per expert (D or 2F)
+  int32_t m_tiles;          // wgrad: m_total / 128
 };
 
 struct TileInfo {
@@ -118,6 +156,23 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a,
     ti.swap_n = 0;
     return ti;
   }
+  if (ModeInfo<MODE>::wgrad) {
+    const int per_e = a.m_tiles * a.n_tiles;
+    const int e = t / per_e;
+    const int local = t - e * per_e;
+    const int n = local / a.m_tiles;
+    const int m = local - n * a.m_tiles;
+    ti.split = 0;
+    ti.swap_n = 0;
+    ti.a_row = e * a.m_total + m * kBM;   // output row of the tile
+    ti.rows = kBM;
+    ti.b_row = m * kBM;                    // A's MN coordinate
+    ti.b_row2 = 0;
+    ti.out_col = n * 256;                  // B's MN coordinate
+    ti.kb_begin = __ldg(a.offsets + e) >> 6;
+    ti.kb_end = __ldg(a.offsets + e + 1) >> 6;
+    return ti;
+  }
   // binary search: the expert whose tile range holds t
   int lo = 0, hi = a.groups - 1;
   while (lo < hi) {
@@ -134,13 +189,20 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a,
   ti.split = 0;
   ti.a_row = row0 + m * kBM;
   ti.rows = min(kBM, cnt - m * kBM);
-  ti.swap_n = ti.rows <= kBM - 16 ? (ti.rows + 15) & ~15 : 0;
+  ti.swap_n = ModeInfo<MODE>::swap_tails && ti.rows <= kBM - 16
+                  ? (ti.rows + 15) & ~15
+                  : 0;
   ti.kb_begin = 0;
   ti.kb_end = a.k_blocks;
-  if (MODE == kUp) {
+  if (ModeInfo<MODE>::gate_up) {
     ti.b_row = e * a.b_rows_per_group + n * 128;
     ti.b_row2 = e * a.b_rows_per_group + a.F + n * 128;
     ti.out_col = n * 128;
+  } else if (ModeInfo<MODE>::b_mn) {
+    // MN-major B: b_row is the expert's first K row in B's row space
+    ti.b_row = e * a.b_rows_per_group;
+    ti.b_row2 = 0;
+    ti.out_col = n * 256;
   } else {
     ti.b_row = e * a.b_rows_per_group + n * 256;
     ti.b_row2 = 0;
@@ -188,6 +250,29 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
     }
     return;
   }
+  if (ModeInfo<MODE>::wgrad) {
+    // fp32 weight gradient rows; an expert with no token rows gets zeros
+    float* out = reinterpret_cast<float*>(a.out) +
+                 static_cast<int64_t>(ti.a_row + r) * a.out_ld + ti.out_col;
+    const bool empty = ti.kb_end <= ti.kb_begin;
+#pragma unroll 1
+    for (int c = 0; c < 256; c += 32) {
+      float v[32];
+      if (empty) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+      } else {
+        tmem_ld32(tmem_row + c, v);
+      }
+      if (ti.out_col + c < a.out_cols) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(out + c + i) =
+              make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      }
+    }
+    return;
+  }
   const int64_t grow = static_cast<int64_t>(ti.a_row) + r;
   const bool valid = r < ti.rows && grow >= 0 && grow < a.M;
   if (MODE == kRoute) {
@@ -227,7 +312,45 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
           st_v4(out + c + i, Vec16<__nv_bfloat16>::from_f32(h + i));
       }
     }
+  } else if (MODE == kUpBwd) {
+    // recomputed gate g and up u; with dH: dU = dH * SiLU(g),
+    // dG = dH * u * SiLU'(g), SiLU'(g) = s (1 + g (1 - s)), s = sigmoid(g);
+    // H = SiLU(g) * u for the W2 gradient
+    const int64_t F = a.F;
+    const __nv_bfloat16* dh = reinterpret_cast<const __nv_bfloat16*>(
+                                  a.aux_in) + grow * F + ti.out_col;
+    __nv_bfloat16* dgu = reinterpret_cast<__nv_bfloat16*>(a.out) +
+                         grow * 2 * F + ti.out_col;
+    __nv_bfloat16* hout = reinterpret_cast<__nv_bfloat16*>(a.out2) +
+                          grow * F + ti.out_col;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      float g[32], u[32];
+      tmem_ld32(tmem_row + c, g);
+      tmem_ld32(tmem_row + 128 + c, u);
+      if (valid) {
+        float d[32], dg[32], du[32], h[32];
+#pragma unroll
+        for (int i = 0; i < 32; i += 8)
+          Vec16<__nv_bfloat16>::to_f32(ld_nc_v4(dh + c + i), d + i);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float sg = 1.0f / (1.0f + __expf(-g[i]));
+          const float sl = g[i] * sg;
+          du[i] = d[i] * sl;
+          dg[i] = d[i] * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
+          h[i] = sl * u[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+          st_v4(dgu + c + i, Vec16<__nv_bfloat16>::from_f32(dg + i));
+          st_v4(dgu + F + c + i, Vec16<__nv_bfloat16>::from_f32(du + i));
+          st_v4(hout + c + i, Vec16<__nv_bfloat16>::from_f32(h + i));
+        }
+      }
+    }
   } else {
+    // kDown, kDH, kDX: 256 bf16 columns
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) +
                          grow * a.out_ld + ti.out_col;
 #pragma unroll 1
@@ -290,7 +413,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmB);
   }
   // tile prefix over experts (grouped modes)
-  if (MODE != kRoute) {
+  if (ModeInfo<MODE>::wgrad) {
+    if (warp == 2) {
+      // every expert segment must start on a 64-row boundary (the K blocks
+      // of one expert never reach into the next)
+      bool aligned = true;
+      for (int e = lane; e <= a.groups; e += 32)
+        aligned = aligned && (__ldg(a.offsets + e) & 63) == 0;
+      aligned = __all_sync(0xffffffffu, aligned);
+      if (lane == 0) {
+        sh.total_tiles = aligned ? a.groups * a.m_tiles * a.n_tiles : 0;
+        if (!aligned) set_status(a.status, MOE_ERR_INVALID);
+      }
+    }
+  } else if (MODE != kRoute) {
     if (warp == 2) {
       int run = 0;
       for (int base = 0; base < a.groups; base += 32) {
@@ -347,11 +483,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(&sh.full[stage], tx);
           uint8_t* sa = a_tiles + stage * kATileBytes;
           uint8_t* sb = b_tiles + static_cast<size_t>(stage) * b_tile_bytes;
-          tma_load_2d(sa, &tmA, &sh.full[stage], kb * kBK, ti.a_row);
-          if (MODE == kUp) {
+          if (ModeInfo<MODE>::a_mn) {
+            // two 64-wide MN boxes of 64 K (token) rows
+            tma_load_2d(sa, &tmA, &sh.full[stage], ti.b_row, kb * kBK);
+            tma_load_2d(sa + 8192, &tmA, &sh.full[stage], ti.b_row + 64,
+                        kb * kBK);
+          } else {
+            tma_load_2d(sa, &tmA, &sh.full[stage], kb * kBK, ti.a_row);
+          }
+          if (ModeInfo<MODE>::gate_up) {
             tma_load_2d(sb, &tmB, &sh.full[stage], kb * kBK, ti.b_row);
             tma_load_2d(sb + 128 * 128, &tmB, &sh.full[stage], kb * kBK,
                         ti.b_row2);
+          } else if (ModeInfo<MODE>::b_mn) {
+            // four 64-wide MN boxes; K rows start at the expert's first K
+            // row in B (dgrad) or at the token row itself (wgrad)
+            const int krow = (ModeInfo<MODE>::wgrad ? 0 : ti.b_row) + kb * kBK;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              tma_load_2d(sb + i * 8192, &tmB, &sh.full[stage],
+                          ti.out_col + 64 * i, krow);
           } else {
             tma_load_2d(sb, &tmB, &sh.full[stage], kb * kBK, ti.b_row);
           }
@@ -381,7 +532,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      const uint32_t idesc = umma_idesc_bf16(kBM, a.BN);
+      const uint32_t idesc = umma_idesc_bf16_major(
+          kBM, a.BN, ModeInfo<MODE>::a_mn, ModeInfo<MODE>::b_mn);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -407,13 +559,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sa = smem_u32(a_tiles + stage * kATileBytes);
           const uint32_t sb =
               smem_u32(b_tiles + static_cast<size_t>(stage) * b_tile_bytes);
-          const uint64_t adesc = umma_desc_sw128(sa);
-          const uint64_t bdesc = umma_desc_sw128(sb);
+          // one K step of 16: +32 bytes along a K-major row (+2 in the
+          // >>4 address field), or +16 rows of 128 bytes MN-major (+128)
+          constexpr uint32_t a_step = ModeInfo<MODE>::a_mn ? 128u : 2u;
+          constexpr uint32_t b_step = ModeInfo<MODE>::b_mn ? 128u : 2u;
+          const uint64_t adesc = ModeInfo<MODE>::a_mn ? umma_desc_mn_sw128(sa)
+                                                      : umma_desc_sw128(sa);
+          const uint64_t bdesc = ModeInfo<MODE>::b_mn ? umma_desc_mn_sw128(sb)
+                                                      : umma_desc_sw128(sb);
           if (MODE == kRoute || ti.swap_n == 0) {
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k) {
-              // +32 bytes along K per step: +2 in the >>4 address field
-              umma_bf16(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc,
+              umma_bf16(d_tmem, adesc + a_step * k, bdesc + b_step * k, idesc,
                         (kb > ti.kb_begin || k > 0) ? 1u : 0u);
             }
           } else {

@@ -170,6 +170,95 @@ class MoELayer:
                       self.dst_row_padded, gate, out, stream)
         return out
 
+    # ---------------------------------------------------------- training
+    ALIGN = 64
+
+    def _train_buffers(self):
+        if getattr(self, "_train", None) is not None:
+            return self._train
+        T, D, E, k, F = self.T, self.D, self.E, self.k, self.F
+        P = T * k
+        rows = P + (self.ALIGN - 1) * E
+        dev = self.device
+        i32 = dict(dtype=torch.int32, device=dev)
+        b = dict(rows=rows,
+                 dst_a=torch.empty(P, **i32),
+                 off_a=torch.empty(E + 1, **i32),
+                 xa=torch.empty((rows, D), dtype=self.dtype, device=dev),
+                 dga=torch.empty((rows, D), dtype=self.dtype, device=dev),
+                 dxa=torch.empty((rows, D), dtype=self.dtype, device=dev),
+                 dgate=torch.empty((T, k), dtype=torch.float32, device=dev),
+                 dlogits=torch.empty((T, E), dtype=torch.float32, device=dev),
+                 dx=torch.empty((T, D), dtype=self.dtype, device=dev),
+                 dw_r=torch.empty((E, D), dtype=torch.float32, device=dev))
+        if self.identity:
+            b["ya"] = b["xa"]
+        else:
+            b["ya"] = torch.empty((rows, D), dtype=self.dtype, device=dev)
+            b["ffn_ws"] = self._bytes(L.moe_grouped_ffn_workspace_size(
+                E, D, F, rows, self.dcode))
+            b["bwd_ws"] = self._bytes(
+                L.moe_grouped_ffn_backward_workspace_size(E, D, F, rows,
+                                                          self.dcode))
+            b["dw13"] = torch.empty((E, 2 * F, D), dtype=torch.float32,
+                                    device=dev)
+            b["dw2"] = torch.empty((E, D, F), dtype=torch.float32,
+                                   device=dev)
+        if self.logits is None:
+            self.logits = torch.empty((T, E), dtype=torch.float32,
+                                      device=dev)
+        self._train = b
+        return b
+
+    def forward_train(self, x, stream=None):
+        """The forward pass on the 64-row aligned training layout, keeping
+        what the backward pass needs (x, logits, routing, Xa, Ya)."""
+        b = self._train_buffers()
+        E, D = self.E, self.D
+        self.route(x, stream)
+        self.dispatch_layout(None, stream)
+        L.moe_aligned_layout(self.T, self.k, E, self.ALIGN, self.topk_idx,
+                             self.dst_row, self.expert_offsets, b["dst_a"],
+                             b["off_a"], self.status, stream)
+        L.moe_aligned_fill(E, D, self.dcode, self.expert_offsets, b["off_a"],
+                           b["xa"], stream)
+        L.moe_permute(self.T, self.k, D, self.dcode, x, b["dst_a"], b["xa"],
+                      stream)
+        if not self.identity:
+            L.moe_grouped_ffn(E, D, self.F, b["rows"], self.dcode, b["xa"],
+                              b["off_a"], self.w13, self.w2, b["ya"],
+                              b["ffn_ws"], self.status, stream)
+        L.moe_combine(self.T, self.k, D, self.dcode, b["ya"], b["dst_a"],
+                      self.topk_gate, self.y, stream)
+        self._x = x
+        return self.y
+
+    def backward(self, dy, stream=None):
+        """Gradients of sum(dy * y) for the last forward_train: returns dx
+        [T, D] (dtype), dw_r [E, D], dw13 [E, 2F, D], dw2 [E, D, F] (fp32;
+        None for identity experts)."""
+        b = self._train
+        E, D = self.E, self.D
+        L.moe_combine_backward(self.T, self.k, D, self.dcode, dy, b["ya"],
+                               b["dst_a"], self.topk_gate, b["dga"],
+                               b["dgate"], stream)
+        L.moe_aligned_fill(E, D, self.dcode, self.expert_offsets, b["off_a"],
+                           b["dga"], stream)
+        dxa = b["dga"]
+        if not self.identity:
+            L.moe_grouped_ffn_backward(E, D, self.F, b["rows"], self.dcode,
+                                       b["xa"], b["dga"], b["off_a"],
+                                       self.w13, self.w2, b["dxa"],
+                                       b["dw13"], b["dw2"], b["bwd_ws"],
+                                       self.status, stream)
+            dxa = b["dxa"]
+        L.moe_permute_backward(self.T, self.k, D, self.dcode, dxa,
+                               b["dst_a"], b["dx"], stream)
+        L.moe_route_backward(self.cfg, self._x, self.w_r, self.logits,
+                             self.topk_idx, b["dgate"], b["dlogits"],
+                             b["dw_r"], b["dx"], self.status, stream)
+        return (b["dx"], b["dw_r"], b.get("dw13"), b.get("dw2"))
+
     # ---------------------------------------------------------- layer
     def forward(self, x, topk_idx=None, topk_gate=None, y=None, stream=None):
         """y = MoE(x) for x [T, D] on the device.  With topk_idx/topk_gate

@@ -358,6 +358,117 @@ MOE_API moe_status moe_pad_fill(int32_t E, int32_t capacity, int32_t D,
                                 int32_t dtype, const int32_t* expert_counts,
                                 void* buf, moe_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Backward pass ("Expert Parallelism in LLMs", Backward Pass Symmetry: the
+ * upstream gradient dL/dy is dispatched to the experts along the forward
+ * dispatch pattern, the experts form their weight gradients and input
+ * gradients, and the input gradients return along the combine pattern).
+ * The routing decision is held fixed; gradients flow through the gates and
+ * the experts.  Order of calls for one layer:
+ *   moe_aligned_layout, moe_aligned_fill (forward rows Xa on 64-row
+ *   aligned expert segments), moe_permute / moe_grouped_ffn / moe_combine on
+ *   that layout, then
+ *   moe_combine_backward -> moe_aligned_fill(dYa) ->
+ *   moe_grouped_ffn_backward -> moe_permute_backward -> moe_route_backward.
+ * ------------------------------------------------------------------------ */
+
+/* moe_aligned_layout -- the training layout: expert e's rows start at
+ * offsets_aligned[e], the exclusive scan of its kept count rounded up to
+ * `align` (64 for moe_grouped_ffn_backward), so that no block of `align`
+ * rows holds two experts.
+ *     dst_row_aligned[p] = offsets_aligned[e] + (dst_row[p] - offsets[e])
+ *   topk_idx, dst_row [T*k] int32 in; expert_offsets [E+1] int32 in (the
+ *   compact layout's); dst_row_aligned [T*k] out (-1 if dropped);
+ *   offsets_aligned [E+1] out.  Rows: offsets_aligned[E] <= T*k + (align-1)*E.
+ * Requires 1 <= align <= 1024 and E <= 1024. */
+MOE_API moe_status moe_aligned_layout(int32_t T, int32_t k, int32_t E,
+                                      int32_t align, const int32_t* topk_idx,
+                                      const int32_t* dst_row,
+                                      const int32_t* expert_offsets,
+                                      int32_t* dst_row_aligned,
+                                      int32_t* offsets_aligned,
+                                      int32_t* status, moe_stream_t stream);
+
+/* moe_aligned_fill -- zero the padding rows of an aligned buffer: rows
+ * [offsets_aligned[e] + count_e, offsets_aligned[e+1]) for every expert,
+ * count_e = expert_offsets[e+1] - expert_offsets[e].
+ *   buf [offsets_aligned[E], D] dtype in/out, 16-byte aligned */
+MOE_API moe_status moe_aligned_fill(int32_t E, int32_t D, int32_t dtype,
+                                    const int32_t* expert_offsets,
+                                    const int32_t* offsets_aligned, void* buf,
+                                    moe_stream_t stream);
+
+/* moe_combine_backward -- backward of moe_combine: for every kept pair
+ * (t, j) with row r = dst_row[t*k + j]:
+ *     dyp[r]          = topk_gate[t, j] * dy[t]      (dtype)
+ *     dgate[t, j]     = dy[t] . yp[r]                (fp32 accumulation)
+ * and dgate = 0 for a dropped pair.  Rows of dyp not named by dst_row are
+ * left unwritten (moe_aligned_fill zeroes an aligned buffer's padding).
+ *   dy [T, D], yp [rows, D], dyp [rows, D] dtype; dgate [T, k] fp32 out */
+MOE_API moe_status moe_combine_backward(int32_t T, int32_t k, int32_t D,
+                                        int32_t dtype, const void* dy,
+                                        const void* yp, const int32_t* dst_row,
+                                        const float* topk_gate, void* dyp,
+                                        float* dgate, moe_stream_t stream);
+
+/* moe_permute_backward -- backward of moe_permute:
+ *     dx[t] = sum over kept slots j of dxp[dst_row[t*k + j]]
+ * (fp32 accumulation in slot order, rounded once to dtype; zeros for a
+ * token with no kept pair).  dxp [rows, D], dx [T, D] dtype. */
+MOE_API moe_status moe_permute_backward(int32_t T, int32_t k, int32_t D,
+                                        int32_t dtype, const void* dxp,
+                                        const int32_t* dst_row, void* dx,
+                                        moe_stream_t stream);
+
+/* Bytes of scratch moe_grouped_ffn_backward needs: dH [max_rows, F],
+ * dGU [max_rows, 2F] and H [max_rows, F] in bf16. */
+MOE_API size_t moe_grouped_ffn_backward_workspace_size(int32_t E, int32_t D,
+                                                       int32_t F,
+                                                       int32_t max_rows,
+                                                       int32_t dtype);
+
+/* moe_grouped_ffn_backward -- backward of moe_grouped_ffn on the aligned
+ * layout (every expert_offsets[e] a multiple of 64; padding rows of xp and
+ * dyp zero).  For expert e and its rows, with G = xp W1_e^T, U = xp W3_e^T
+ * recomputed:
+ *     dH   = dyp W2_e
+ *     dG   = dH * U * SiLU'(G),  dU = dH * SiLU(G),  H = SiLU(G) * U
+ *     dxp  = dG W1_e + dU W3_e                         (dtype out)
+ *     dw2[e]  = dyp^T H,  dw13[e] = [dG | dU]^T xp      (fp32 out)
+ * An expert with no rows gets zero weight gradients.  All five GEMMs run on
+ * the tcgen05 tensor cores (bf16 in, fp32 accumulate).
+ *   xp, dyp [max_rows, D] bf16, 256-byte aligned; w13 [E, 2F, D] and
+ *   w2 [E, D, F] bf16 (the forward weights); dxp [max_rows, D] bf16 out;
+ *   dw13 [E, 2F, D] and dw2 [E, D, F] fp32 out, 16-byte aligned.
+ * MOE_BF16 only, D % 128 == 0 and F % 128 == 0 (else MOE_ERR_UNSUPPORTED).
+ * Unaligned offsets are detected on the device: MOE_ERR_INVALID in
+ * `status` and no weight gradient is written. */
+MOE_API moe_status moe_grouped_ffn_backward(
+    int32_t E, int32_t D, int32_t F, int32_t max_rows, int32_t dtype,
+    const void* xp, const void* dyp, const int32_t* expert_offsets,
+    const void* w13, const void* w2, void* dxp, float* dw13, float* dw2,
+    void* workspace, size_t workspace_bytes, int32_t* status,
+    moe_stream_t stream);
+
+/* moe_route_backward -- backward of the router for the decision moe_route
+ * made: from dgate [T, k] (moe_combine_backward's output)
+ *     dlogits[t]  per score mode (softmax over the selected logits; softmax
+ *                 over all E taken at the selected experts; selected
+ *                 sigmoid scores normalised to sum 1 -- the selection bias
+ *                 has no gradient path)
+ *     dw_r        = dlogits^T x                   (fp32, may be NULL)
+ *     dx         += dlogits w_r                   (dtype, in place, may be
+ *                                                  NULL)
+ *   cfg host pointer (as for moe_route); x [T, D], w_r [E, D] dtype;
+ *   logits [T, E] fp32 (moe_route's logits_out); topk_idx [T, k];
+ *   dlogits [T, E] fp32 out; dw_r [E, D] fp32 out. */
+MOE_API moe_status moe_route_backward(const moe_route_cfg* cfg, const void* x,
+                                      const void* w_r, const float* logits,
+                                      const int32_t* topk_idx,
+                                      const float* dgate, float* dlogits,
+                                      float* dw_r, void* dx, int32_t* status,
+                                      moe_stream_t stream);
+
 /* Test hook for the bounded-wait machinery: launches one CTA that waits on
  * a shared-memory barrier nothing arrives on, gives up after `limit_ns`
  * nanoseconds, writes MOE_ERR_TIMEOUT into `status` and returns. */

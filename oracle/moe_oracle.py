@@ -653,3 +653,27 @@ def moe_backward(x, w_r, dy, k, E, R, mode, w13=None, w2=None,
     dx += dlogits @ np.asarray(w_r, dtype=np.float64)
     return dict(dx=dx, dw_r=dw_r, dw13=dw13, dw2=dw2, dgate=dgate,
                 dlogits=dlogits, dyp=dyp, dxp=dxp, forward=fw)
+
+
+def aligned_layout(layout, E, align):
+    """The training layout: expert e's rows start at the exclusive scan of
+    its kept count rounded up to `align`, in the compact layout's order, so
+    that no block of `align` rows holds two experts.  Returns
+    dst_row_aligned [P] (-1 if dropped) and offsets_aligned [E+1]."""
+    counts = np.asarray(layout["counts"])
+    off = np.asarray(layout["offsets"])
+    dst = np.asarray(layout["dst_row"])
+    idx_of_row = {}
+    for e in range(E):
+        for r in range(int(off[e]), int(off[e + 1])):
+            idx_of_row[r] = e
+    off_a = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        c = int(counts[e])
+        off_a[e + 1] = off_a[e] + (c + align - 1) // align * align
+    dst_a = np.full(dst.shape[0], -1, dtype=np.int64)
+    for p, r in enumerate(dst):
+        if int(r) >= 0:
+            e = idx_of_row[int(r)]
+            dst_a[p] = off_a[e] + (int(r) - int(off[e]))
+    return dict(dst_row_aligned=dst_a, offsets_aligned=off_a)

@@ -202,3 +202,30 @@ def test_mutation_padding_not_zeroed_is_caught(monkeypatch):
         return out
     monkeypatch.setattr(O, "permute_padded", ones)
     assert _fails(lambda: test_padded_layout_matches_compact(12))
+
+
+# ------------------------------------------------------ aligned layout -----
+@pytest.mark.parametrize("align", [1, 8, 64])
+def test_aligned_layout_invariants(align):
+    rng = np.random.default_rng(align)
+    T, k, E = 300, 2, 7
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    idx[:50, 0] = 3                         # a heavy expert
+    lay = O.dispatch_layout(idx, E, 1, 90)
+    al = O.aligned_layout(lay, E, align)
+    off_a = al["offsets_aligned"]
+    assert (off_a % align == 0).all()
+    # align = 1 is the compact layout itself
+    if align == 1:
+        assert off_a.tolist() == lay["offsets"].tolist()
+        assert al["dst_row_aligned"].tolist() == lay["dst_row"].tolist()
+    dst = al["dst_row_aligned"]
+    kept = dst >= 0
+    assert (kept == (lay["dst_row"] >= 0)).all()
+    assert len(set(dst[kept].tolist())) == kept.sum()      # one row each
+    for p in np.flatnonzero(kept):
+        e = int(idx.reshape(-1)[p])
+        assert off_a[e] <= dst[p] < off_a[e] + lay["counts"][e]
+        # same position inside the expert as in the compact layout
+        assert dst[p] - off_a[e] == lay["dst_row"][p] - lay["offsets"][e]
+    assert off_a[E] <= T * k + (align - 1) * E
