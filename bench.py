@@ -540,7 +540,8 @@ def run_train(args, local_rank, workload):
         rec(4)
         L.moe_route_backward(layer.cfg, x, layer.w_r, layer.logits,
                              layer.topk_idx, b["dgate"], b["dlogits"],
-                             b["dw_r"], b["dx"], layer.status, stream)
+                             b["dw_r"], b["dx"], b["route_bwd_ws"],
+                             layer.status, stream)
         rec(5)
 
     layer._x = x

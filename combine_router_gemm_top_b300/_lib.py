@@ -44,6 +44,7 @@ EXPORTED = ["moe_route_workspace_size", "moe_route",
             "moe_aligned_fill", "moe_combine_backward",
             "moe_permute_backward", "moe_grouped_ffn_backward_workspace_size",
             "moe_grouped_ffn_backward", "moe_route_backward",
+            "moe_route_backward_workspace_size",
             "moe_status_str", "moe_abi_version"]
 ABI_VERSION = 1
 
@@ -107,7 +108,9 @@ _SIGS = {
                                         _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                         _vp, _sz, _vp, _vp]),
     "moe_route_backward": (_i32, [ctypes.POINTER(RouteCfg), _vp, _vp, _vp,
-                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+                                  _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
+                                  _vp]),
+    "moe_route_backward_workspace_size": (_sz, [ctypes.POINTER(RouteCfg)]),
     "moe_selftest_bounded_wait": (_i32, [_vp, _u64, _vp]),
     "moe_selftest_sigmoid_key": (_i32, [_vp, _vp, _i32, _vp]),
     "moe_status_str": (ctypes.c_char_p, [_i32]),
@@ -335,12 +338,19 @@ def moe_grouped_ffn_backward(E, D, F, max_rows, dtype, xp, dyp,
         _p(status), _stream(stream)), "moe_grouped_ffn_backward")
 
 
+def moe_route_backward_workspace_size(cfg) -> int:
+    return load().moe_route_backward_workspace_size(ctypes.byref(cfg))
+
+
 def moe_route_backward(cfg, x, w_r, logits, topk_idx, dgate, dlogits, dw_r,
-                       dx, status, stream=None):
+                       dx, workspace, status, stream=None):
+    nbytes = 0 if workspace is None else \
+        workspace.numel() * workspace.element_size()
     _check(load().moe_route_backward(ctypes.byref(cfg), _p(x), _p(w_r),
                                      _p(logits), _p(topk_idx), _p(dgate),
                                      _p(dlogits), _p(dw_r), _p(dx),
-                                     _p(status), _stream(stream)),
+                                     _p(workspace), nbytes, _p(status),
+                                     _stream(stream)),
            "moe_route_backward")
 
 

@@ -426,10 +426,17 @@ moe_status moe_grouped_ffn_backward(
                                      num_sms());
 }
 
+size_t moe_route_backward_workspace_size(const moe_route_cfg* cfg) {
+  if (!route_cfg_ok(cfg)) return 0;
+  const size_t b = route_bwd_ws_bytes(cfg->T, cfg->D, cfg->E, num_sms());
+  return b > 0 ? b : 16;
+}
+
 moe_status moe_route_backward(const moe_route_cfg* cfg, const void* x,
                               const void* w_r, const float* logits,
                               const int32_t* topk_idx, const float* dgate,
                               float* dlogits, float* dw_r, void* dx,
+                              void* workspace, size_t workspace_bytes,
                               int32_t* status, moe_stream_t stream) {
   (void)status;
   if (!route_cfg_ok(cfg)) return MOE_ERR_INVALID;
@@ -439,10 +446,16 @@ moe_status moe_route_backward(const moe_route_cfg* cfg, const void* x,
     return MOE_ERR_INVALID;
   if (dw_r != nullptr && x == nullptr) return MOE_ERR_INVALID;
   if (dx != nullptr && w_r == nullptr) return MOE_ERR_INVALID;
+  const int sms = num_sms();
+  const size_t need = route_bwd_ws_bytes(cfg->T, cfg->D, cfg->E, sms);
+  if (dw_r != nullptr && need > 0 &&
+      (workspace == nullptr || workspace_bytes < need ||
+       !aligned(workspace, 16)))
+    return MOE_ERR_INVALID;
   return launch_route_backward(cfg->T, cfg->D, cfg->E, cfg->k, cfg->score,
                                cfg->dtype, x, w_r, logits, topk_idx, dgate,
-                               dlogits, dw_r, dx,
-                               reinterpret_cast<cudaStream_t>(stream));
+                               dlogits, dw_r, dx, workspace,
+                               reinterpret_cast<cudaStream_t>(stream), sms);
 }
 
 moe_status moe_selftest_bounded_wait(int32_t* status, uint64_t limit_ns,

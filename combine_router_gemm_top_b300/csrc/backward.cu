@@ -304,65 +304,94 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
   }
 }
 
-// dW_r[e, d] = sum_t dl[t, e] x[t, d]: block (256 d, 8 experts), tokens in
-// a fixed order.
-template <typename T>
+// dW_r[e, d] = sum_t dl[t, e] x[t, d].  Block = 256 columns d x EB experts
+// over one slice of the tokens; slices are summed in a fixed order by
+// dwr_reduce_kernel (or written directly when there is one slice).
+template <typename T, int EB>
 __global__ void __launch_bounds__(256)
-    dwr_kernel(int Tn, int E, int D, const float* __restrict__ dl,
-               const T* __restrict__ x, float* __restrict__ dwr) {
-  __shared__ float s_dl[64][8];
+    dwr_kernel(int Tn, int E, int D, int t_per_slice,
+               const float* __restrict__ dl, const T* __restrict__ x,
+               float* __restrict__ out) {
+  __shared__ float s_dl[32][EB];
   const int d = blockIdx.x * 256 + threadIdx.x;
-  const int e0 = blockIdx.y * 8;
-  float acc[8];
+  const int e0 = blockIdx.y * EB;
+  const int ts = blockIdx.z * t_per_slice;
+  const int te = min(Tn, ts + t_per_slice);
+  float acc[EB];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int t0 = 0; t0 < Tn; t0 += 64) {
+  for (int i = 0; i < EB; ++i) acc[i] = 0.0f;
+  for (int t0 = ts; t0 < te; t0 += 32) {
     __syncthreads();
-    for (int i = threadIdx.x; i < 64 * 8; i += 256) {
-      const int tt = t0 + i / 8, ee = e0 + i % 8;
-      s_dl[i / 8][i % 8] = tt < Tn && ee < E ? dl[static_cast<int64_t>(tt) * E + ee] : 0.0f;
+    for (int i = threadIdx.x; i < 32 * EB; i += 256) {
+      const int tt = t0 + i / EB, ee = e0 + i % EB;
+      s_dl[i / EB][i % EB] =
+          tt < te && ee < E ? dl[static_cast<int64_t>(tt) * E + ee] : 0.0f;
     }
     __syncthreads();
     if (d < D) {
-      const int tn = min(64, Tn - t0);
+      const int tn = min(32, te - t0);
       for (int i = 0; i < tn; ++i) {
-        const float xv = static_cast<float>(x[static_cast<int64_t>(t0 + i) * D + d]);
+        const float xv =
+            static_cast<float>(x[static_cast<int64_t>(t0 + i) * D + d]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(s_dl[i][j], xv, acc[j]);
+        for (int j = 0; j < EB; ++j) acc[j] = fmaf(s_dl[i][j], xv, acc[j]);
       }
     }
   }
   if (d < D) {
+    float* o = out + static_cast<int64_t>(blockIdx.z) * E * D;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (e0 + j < E) dwr[static_cast<int64_t>(e0 + j) * D + d] = acc[j];
+    for (int j = 0; j < EB; ++j)
+      if (e0 + j < E) o[static_cast<int64_t>(e0 + j) * D + d] = acc[j];
   }
 }
 
-// dx[t, d] += sum_e dl[t, e] W_r[e, d]: block (256 d, 8 tokens).
+__global__ void dwr_reduce_kernel(int64_t n, int slices,
+                                  const float* __restrict__ part,
+                                  float* __restrict__ dwr) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float s = 0.0f;
+  for (int k = 0; k < slices; ++k) s += part[k * n + i];
+  dwr[i] = s;
+}
+
+// dx[t, d] += sum_e dl[t, e] W_r[e, d]: block = 256 columns d x 32 tokens.
+// The block's dl values sit in shared memory expert-major, 32 tokens (plus
+// 4 floats of padding) per expert, so each thread reads them as float4.
+constexpr int kDxLd = 36;
+
 template <typename T>
 __global__ void __launch_bounds__(256)
     dx_router_kernel(int Tn, int E, int D, const float* __restrict__ dl,
                      const T* __restrict__ wr, T* __restrict__ dx) {
-  extern __shared__ float s_dlt[];   // [8][E]
+  extern __shared__ float s_dlt[];   // [E][kDxLd]
   const int d = blockIdx.x * 256 + threadIdx.x;
-  const int t0 = blockIdx.y * 8;
-  for (int i = threadIdx.x; i < 8 * E; i += 256) {
-    const int tt = t0 + i / E;
-    s_dlt[i] = tt < Tn ? dl[static_cast<int64_t>(tt) * E + i % E] : 0.0f;
+  const int t0 = blockIdx.y * 32;
+  for (int i = threadIdx.x; i < 32 * E; i += 256) {
+    const int tt = i / E, ee = i - tt * E;
+    s_dlt[ee * kDxLd + tt] =
+        t0 + tt < Tn ? dl[static_cast<int64_t>(t0 + tt) * E + ee] : 0.0f;
   }
   __syncthreads();
   if (d >= D) return;
-  float acc[8];
+  float acc[32];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
   for (int e = 0; e < E; ++e) {
     const float w = static_cast<float>(wr[static_cast<int64_t>(e) * D + d]);
+    const float4* q = reinterpret_cast<const float4*>(s_dlt + e * kDxLd);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = fmaf(s_dlt[j * E + e], w, acc[j]);
+    for (int j = 0; j < 8; ++j) {
+      const float4 v = q[j];
+      acc[4 * j] = fmaf(v.x, w, acc[4 * j]);
+      acc[4 * j + 1] = fmaf(v.y, w, acc[4 * j + 1]);
+      acc[4 * j + 2] = fmaf(v.z, w, acc[4 * j + 2]);
+      acc[4 * j + 3] = fmaf(v.w, w, acc[4 * j + 3]);
+    }
   }
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < 32; ++j) {
     const int tt = t0 + j;
     if (tt < Tn) {
       T* p = dx + static_cast<int64_t>(tt) * D + d;
@@ -371,14 +400,56 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Token slices for dW_r: enough blocks to cover the SMs twice.
+struct DwrPlan {
+  int eb, slices, t_per_slice;
+};
+static DwrPlan dwr_plan(int T, int E, int D, int num_sms) {
+  DwrPlan p;
+  p.eb = E >= 32 ? 32 : 8;
+  const int64_t base = ceil_div(D, 256) * ceil_div(E, p.eb);
+  int64_t s = ceil_div(2 * num_sms, base);
+  const int64_t max_s = ceil_div(T, 32);
+  s = s < 1 ? 1 : (s > 64 ? 64 : s);
+  s = s > max_s ? max_s : s;
+  p.t_per_slice = static_cast<int>(ceil_div(ceil_div(T, s), 32) * 32);
+  p.slices = static_cast<int>(ceil_div(T, p.t_per_slice));
+  if (p.slices < 1) p.slices = 1;
+  return p;
+}
+
+size_t route_bwd_ws_bytes(int T, int D, int E, int num_sms) {
+  const DwrPlan p = dwr_plan(T, E, D, num_sms);
+  return p.slices > 1 ? static_cast<size_t>(p.slices) * E * D * sizeof(float)
+                      : 0;
+}
+
+template <typename T>
+static void launch_dwr(const DwrPlan& p, int Tn, int E, int D,
+                       const float* dl, const T* x, float* dwr, float* ws,
+                       cudaStream_t stream) {
+  float* out = p.slices > 1 ? ws : dwr;
+  const dim3 g(static_cast<unsigned>(ceil_div(D, 256)),
+               static_cast<unsigned>(ceil_div(E, p.eb)),
+               static_cast<unsigned>(p.slices));
+  if (p.eb == 32)
+    dwr_kernel<T, 32><<<g, 256, 0, stream>>>(Tn, E, D, p.t_per_slice, dl, x, out);
+  else
+    dwr_kernel<T, 8><<<g, 256, 0, stream>>>(Tn, E, D, p.t_per_slice, dl, x, out);
+  if (p.slices > 1) {
+    const int64_t n = static_cast<int64_t>(E) * D;
+    dwr_reduce_kernel<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0,
+                        stream>>>(n, p.slices, ws, dwr);
+  }
+}
+
 moe_status launch_route_backward(int T, int D, int E, int k, int score,
                                  int dtype, const void* x, const void* w_r,
                                  const float* logits, const int32_t* topk_idx,
                                  const float* dgate, float* dlogits,
-                                 float* dw_r, void* dx, cudaStream_t stream) {
-  if (T == 0) {
-    return MOE_OK;
-  }
+                                 float* dw_r, void* dx, void* ws,
+                                 cudaStream_t stream, int num_sms) {
+  if (T == 0) return MOE_OK;
   const unsigned g1 = static_cast<unsigned>(ceil_div(T, kBwdWarps));
   const int ni = static_cast<int>(ceil_div(E, 32));
   if (ni <= 1)
@@ -389,23 +460,22 @@ moe_status launch_route_backward(int T, int D, int E, int k, int score,
     dlogits_kernel<4><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits);
   else
     dlogits_kernel<8><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits);
-  const dim3 gw(static_cast<unsigned>(ceil_div(D, 256)),
-                static_cast<unsigned>(ceil_div(E, 8)));
+  const DwrPlan p = dwr_plan(T, E, D, num_sms);
   const dim3 gx(static_cast<unsigned>(ceil_div(D, 256)),
-                static_cast<unsigned>(ceil_div(T, 8)));
-  const size_t smem = static_cast<size_t>(8) * E * sizeof(float);
+                static_cast<unsigned>(ceil_div(T, 32)));
+  const size_t smem = static_cast<size_t>(kDxLd) * E * sizeof(float);
   if (dtype == MOE_BF16) {
     if (dw_r != nullptr)
-      dwr_kernel<__nv_bfloat16><<<gw, 256, 0, stream>>>(
-          T, E, D, dlogits, static_cast<const __nv_bfloat16*>(x), dw_r);
+      launch_dwr(p, T, E, D, dlogits, static_cast<const __nv_bfloat16*>(x),
+                 dw_r, static_cast<float*>(ws), stream);
     if (dx != nullptr)
       dx_router_kernel<__nv_bfloat16><<<gx, 256, smem, stream>>>(
           T, E, D, dlogits, static_cast<const __nv_bfloat16*>(w_r),
           static_cast<__nv_bfloat16*>(dx));
   } else {
     if (dw_r != nullptr)
-      dwr_kernel<float><<<gw, 256, 0, stream>>>(
-          T, E, D, dlogits, static_cast<const float*>(x), dw_r);
+      launch_dwr(p, T, E, D, dlogits, static_cast<const float*>(x), dw_r,
+                 static_cast<float*>(ws), stream);
     if (dx != nullptr)
       dx_router_kernel<float><<<gx, 256, smem, stream>>>(
           T, E, D, dlogits, static_cast<const float*>(w_r),

@@ -89,7 +89,8 @@ static moe_status launch_umma(const CUtensorMap& tmA, const CUtensorMap& tmB,
       return MOE_ERR_CUDA;
     attr_set = true;
   }
-  const size_t smem = umma_gemm_smem_bytes(g.BN, g.stages);
+  const size_t smem =
+      umma_gemm_smem_bytes(g.BN, g.stages, ModeInfo<MODE>::wgrad);
   umma_gemm_kernel<MODE><<<num_sms, kGemmThreads, smem, stream>>>(tmA, tmB, g);
   return launch_status();
 }
@@ -262,8 +263,10 @@ moe_status launch_grouped_ffn_backward(int E, int D, int F, int max_rows,
   s = launch_umma<kDX>(t_dgu, t_w13mn, g, stream, num_sms);
   if (s != MOE_OK) return s;
 
-  // dW2_e = dYp_e^T . H_e   [D, F] per expert, fp32
+  // dW2_e = dYp_e^T . H_e   [D, F] per expert, fp32 (3 stages leave room
+  // for the epilogue's staging tiles)
   g = base;
+  g.stages = 3;
   g.m_total = D;
   g.m_tiles = D / kBM;
   g.n_tiles = static_cast<int>(ceil_div(F, 256));
@@ -276,6 +279,7 @@ moe_status launch_grouped_ffn_backward(int E, int D, int F, int max_rows,
 
   // dW13_e = dGU_e^T . Xp_e   [2F, D] per expert, fp32
   g = base;
+  g.stages = 3;
   g.m_total = 2 * F;
   g.m_tiles = 2 * F / kBM;
   g.n_tiles = static_cast<int>(ceil_div(D, 256));

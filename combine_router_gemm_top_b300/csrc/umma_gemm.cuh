@@ -1,7 +1,7 @@
 // Persistent, warp-specialised tcgen05 GEMM for sm_103a:
 //   C[128 x BN tile] = A[rows, K] . B[cols, K]^T,  bf16 in, fp32 in TMEM.
 //
-// One CTA per SM, 6 warps:
+// One CTA per SM, 10 warps:
 //   warp 0      TMA producer (one elected lane): A and B tiles into a ring of
 //               shared-memory stages (128-byte swizzle), completion counted
 //               on per-stage "full" mbarriers.
@@ -11,8 +11,10 @@
 //               publishes the accumulator ("tfull").  Two accumulators
 //               alternate so the epilogue of tile i overlaps the MMAs of
 //               tile i+1.
-//   warps 2-5   epilogue: tcgen05.ld of their 32 TMEM lanes (one tile row
+//   warps 2-9   epilogue: tcgen05.ld of their 32 TMEM lanes (one tile row
 //               per thread), the mode's math, 16-byte stores, then "tempty".
+//               Two warps share each lane quarter and take alternate column
+//               chunks, so stores issue from 8 warps.
 //
 // Three modes share the pipeline and differ in tile scheduling, the B
 // operand rows and the epilogue:
@@ -84,9 +86,14 @@ constexpr int kBM = 128;          // tile rows (TMEM lanes)
 constexpr int kBK = 64;           // K elements per stage (one 128-byte row)
 constexpr int kUmmaK = 16;        // K per tcgen05.mma for 16-bit inputs
 constexpr int kMaxStages = 8;
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 8;      // two per TMEM lane quarter
+constexpr int kGemmThreads = 64 + kEpiWarps * 32;
 constexpr int kMaxGroups = 1024;  // experts the grouped scheduler handles
 constexpr uint32_t kATileBytes = kBM * kBK * 2;
+// Weight-gradient epilogue: a 32 x 32 fp32 staging tile per epilogue warp,
+// rows padded to 36 floats (16-byte aligned, conflict-free float4 access).
+constexpr int kStageLd = 36;
+constexpr size_t kStageBytes = static_cast<size_t>(kEpiWarps) * 32 * kStageLd * 4;
 
 struct GemmArgs {
   int32_t M;                // route: T ; grouped: rows allocated (max_rows)
@@ -215,11 +222,13 @@ __device__ __forceinline__ float silu_f32(float g) {
   return g / (1.0f + __expf(-g));
 }
 
-// Epilogue of one tile for the thread owning tile row `r` (TMEM lane r).
+// Epilogue of one tile for the thread owning tile row `r` (TMEM lane r);
+// `half` selects the alternate column chunks this warp handles.
 template <int MODE>
 __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
                                              const TileInfo& ti,
-                                             uint32_t tmem_row, int r) {
+                                             uint32_t tmem_row, int r,
+                                             int half, float* stage) {
   if (MODE != kRoute && ti.swap_n != 0) {
     // swapped tail: TMEM lane r is output feature out_col + r (and, for the
     // down projection, out_col + 128 + r); column j is token row a_row + j
@@ -230,7 +239,7 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
     const bool lo_ok = ti.out_col + r < a.out_cols;
     const bool hi_ok = ti.out_col + 128 + r < a.out_cols;
 #pragma unroll 1
-    for (int c = 0; c < ti.swap_n; c += 16) {
+    for (int c = 16 * half; c < ti.swap_n; c += 32) {
       float v0[16], v1[16];
       tmem_ld16(tmem_row + c, v0);
       tmem_ld16(tmem_row + 128 + c, v1);
@@ -251,12 +260,15 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
     return;
   }
   if (ModeInfo<MODE>::wgrad) {
-    // fp32 weight gradient rows; an expert with no token rows gets zeros
-    float* out = reinterpret_cast<float*>(a.out) +
-                 static_cast<int64_t>(ti.a_row + r) * a.out_ld + ti.out_col;
+    // fp32 weight-gradient rows; an expert with no token rows gets zeros.
+    // Each 32 x 32 chunk goes through this warp's staging tile so that a
+    // store instruction writes four whole 128-byte row segments instead of
+    // one 16-byte piece of 32 different rows.
+    const int lane = r & 31;
+    const int row0 = ti.a_row + (r & ~31);       // the warp's first row
     const bool empty = ti.kb_end <= ti.kb_begin;
 #pragma unroll 1
-    for (int c = 0; c < 256; c += 32) {
+    for (int c = 32 * half; c < 256; c += 64) {
       float v[32];
       if (empty) {
 #pragma unroll
@@ -267,8 +279,21 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
       if (ti.out_col + c < a.out_cols) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(out + c + i) =
+          *reinterpret_cast<float4*>(stage + lane * kStageLd + i) =
               make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        __syncwarp();
+        const int sub = lane >> 3;                // row within a group of 4
+        const int col = (lane & 7) * 4;
+#pragma unroll
+        for (int rr = 0; rr < 32; rr += 4) {
+          const float4 q =
+              *reinterpret_cast<const float4*>(stage + (rr + sub) * kStageLd + col);
+          *reinterpret_cast<float4*>(
+              reinterpret_cast<float*>(a.out) +
+              static_cast<int64_t>(row0 + rr + sub) * a.out_ld + ti.out_col +
+              c + col) = q;
+        }
+        __syncwarp();
       }
     }
     return;
@@ -279,7 +304,7 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
     // partial logits [split][T][E] fp32
     float* out = reinterpret_cast<float*>(a.out) +
                  (static_cast<int64_t>(ti.split) * a.M + grow) * a.E;
-    for (int c = 0; c < a.BN; c += 16) {
+    for (int c = 16 * half; c < a.BN; c += 32) {
       float v[16];
       tmem_ld16(tmem_row + c, v);
       if (valid) {
@@ -299,7 +324,7 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) +
                          grow * a.out_ld + ti.out_col;
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
+    for (int c = 32 * half; c < 128; c += 64) {
       float g[32], u[32];
       tmem_ld32(tmem_row + c, g);
       tmem_ld32(tmem_row + 128 + c, u);
@@ -324,7 +349,7 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
     __nv_bfloat16* hout = reinterpret_cast<__nv_bfloat16*>(a.out2) +
                           grow * F + ti.out_col;
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
+    for (int c = 32 * half; c < 128; c += 64) {
       float g[32], u[32];
       tmem_ld32(tmem_row + c, g);
       tmem_ld32(tmem_row + 128 + c, u);
@@ -354,7 +379,7 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) +
                          grow * a.out_ld + ti.out_col;
 #pragma unroll 1
-    for (int c = 0; c < 256; c += 32) {
+    for (int c = 32 * half; c < 256; c += 64) {
       float v[32];
       tmem_ld32(tmem_row + c, v);
       if (valid && ti.out_col + c < a.out_cols) {
@@ -401,7 +426,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.tfull[i], 1);
-      mbar_init(&sh.tempty[i], 4);
+      mbar_init(&sh.tempty[i], kEpiWarps);
     }
     mbar_init(&sh.drain, 1);
     sh.abort = 0;
@@ -601,9 +626,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue warps 2..5
+    // ---------------- epilogue warps 2..9
     const int quarter = warp & 3;          // TMEM lanes 32*quarter ..
+    const int half = (warp - 2) >> 2;      // alternate column chunks
     const int r = quarter * 32 + lane;     // tile row of this thread
+    float* stage = reinterpret_cast<float*>(
+                       reinterpret_cast<uint8_t*>(&sh) +
+                       ((sizeof(GemmShared) + 15) & ~size_t(15))) +
+                   (warp - 2) * 32 * kStageLd;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       const TileInfo ti = decode_tile<MODE>(a, sh, t);
@@ -618,7 +648,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t tmem_row =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
           acc * a.BN;
-      epilogue_row<MODE>(a, ti, tmem_row, r);
+      epilogue_row<MODE>(a, ti, tmem_row, r, half, stage);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.tempty[acc]);
@@ -635,10 +665,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0 && sh.abort) set_status(a.status, MOE_ERR_TIMEOUT);
 }
 
-// Shared-memory bytes of one launch (tiles + control block + alignment slack).
-inline size_t umma_gemm_smem_bytes(int BN, int stages) {
+// Shared-memory bytes of one launch (tiles + control block + alignment slack
+// + the weight-gradient staging tiles when `staging`).
+inline size_t umma_gemm_smem_bytes(int BN, int stages, bool staging = false) {
   return 1024 + static_cast<size_t>(stages) * (kATileBytes + BN * kBK * 2) +
-         sizeof(GemmShared);
+         ((sizeof(GemmShared) + 15) & ~size_t(15)) +
+         (staging ? kStageBytes : 0);
 }
 
 }  // namespace moe

@@ -190,7 +190,9 @@ class MoELayer:
                  dgate=torch.empty((T, k), dtype=torch.float32, device=dev),
                  dlogits=torch.empty((T, E), dtype=torch.float32, device=dev),
                  dx=torch.empty((T, D), dtype=self.dtype, device=dev),
-                 dw_r=torch.empty((E, D), dtype=torch.float32, device=dev))
+                 dw_r=torch.empty((E, D), dtype=torch.float32, device=dev),
+                 route_bwd_ws=self._bytes(
+                     L.moe_route_backward_workspace_size(self.cfg)))
         if self.identity:
             b["ya"] = b["xa"]
         else:
@@ -256,7 +258,8 @@ class MoELayer:
                                b["dst_a"], b["dx"], stream)
         L.moe_route_backward(self.cfg, self._x, self.w_r, self.logits,
                              self.topk_idx, b["dgate"], b["dlogits"],
-                             b["dw_r"], b["dx"], self.status, stream)
+                             b["dw_r"], b["dx"], b["route_bwd_ws"],
+                             self.status, stream)
         return (b["dx"], b["dw_r"], b.get("dw13"), b.get("dw2"))
 
     # ---------------------------------------------------------- layer

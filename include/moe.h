@@ -461,13 +461,22 @@ MOE_API moe_status moe_grouped_ffn_backward(
  *                                                  NULL)
  *   cfg host pointer (as for moe_route); x [T, D], w_r [E, D] dtype;
  *   logits [T, E] fp32 (moe_route's logits_out); topk_idx [T, k];
- *   dlogits [T, E] fp32 out; dw_r [E, D] fp32 out. */
+ *   dlogits [T, E] fp32 out; dw_r [E, D] fp32 out;
+ *   workspace >= moe_route_backward_workspace_size(cfg) bytes, 16-byte
+ *   aligned (may be NULL when dw_r is NULL).
+ * dw_r and dx are deterministic: fixed-order fp32 sums. */
 MOE_API moe_status moe_route_backward(const moe_route_cfg* cfg, const void* x,
                                       const void* w_r, const float* logits,
                                       const int32_t* topk_idx,
                                       const float* dgate, float* dlogits,
-                                      float* dw_r, void* dx, int32_t* status,
+                                      float* dw_r, void* dx, void* workspace,
+                                      size_t workspace_bytes, int32_t* status,
                                       moe_stream_t stream);
+
+/* Bytes of scratch moe_route_backward needs for dw_r (per-slice partial sums
+ * of the token contraction, added in a fixed order).  Returns 0 for an
+ * invalid cfg. */
+MOE_API size_t moe_route_backward_workspace_size(const moe_route_cfg* cfg);
 
 /* Test hook for the bounded-wait machinery: launches one CTA that waits on
  * a shared-memory barrier nothing arrives on, gives up after `limit_ns`

@@ -236,9 +236,11 @@ def test_route_backward_parity(T, D, E, k, score, groups):
     dwr = torch.full((E, D), float("nan"), device=DEV)
     dx = dx0.to(DEV)
     st = torch.zeros(1, **I32)
+    ws = torch.empty(L.moe_route_backward_workspace_size(cfg),
+                     dtype=torch.uint8, device=DEV)
     L.moe_route_backward(cfg, x.to(DEV), w_r.to(DEV), logits.to(DEV),
                          torch.tensor(idx, device=DEV), dgate.to(DEV), dl,
-                         dwr, dx, st)
+                         dwr, dx, ws, st)
     torch.cuda.synchronize()
     ref_dl = np.stack([O.gate_backward(logits[t].numpy(), idx[t],
                                        dgate[t].numpy(), score)
