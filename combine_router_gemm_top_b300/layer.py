@@ -287,5 +287,56 @@ class MoELayer:
             y_host.copy_(self.y, non_blocking=True)
         return y_host
 
+    def forward_host_stream(self, xs_host, ys_host, stream=None,
+                            topk_idx=None, topk_gate=None):
+        """A stream of batches from pinned host memory through the layer and
+        back: batch i+1's host-to-device copy and batch i-1's device-to-host
+        copy run on their own streams while batch i computes (two device
+        input and output buffers, alternating).  Returns ys_host."""
+        s = stream or torch.cuda.current_stream()
+        if getattr(self, "_stream_bufs", None) is None:
+            self._stream_bufs = dict(
+                x=[torch.empty((self.T, self.D), dtype=self.dtype,
+                               device=self.device) for _ in range(2)],
+                y=[torch.empty((self.T, self.D), dtype=self.dtype,
+                               device=self.device) for _ in range(2)],
+                h2d=torch.cuda.Stream(device=self.device),
+                d2h=torch.cuda.Stream(device=self.device))
+        b = self._stream_bufs
+        h2d, d2h = b["h2d"], b["d2h"]
+        n = len(xs_host)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        x_ready = [ev() for _ in range(n)]
+        x_free = [ev() for _ in range(n)]
+        y_ready = [ev() for _ in range(n)]
+        y_free = [ev() for _ in range(n)]
+        h2d.wait_stream(s)
+        d2h.wait_stream(s)
+
+        def load(i):
+            with torch.cuda.stream(h2d):
+                if i >= 2:
+                    h2d.wait_event(x_free[i - 2])
+                b["x"][i % 2].copy_(xs_host[i], non_blocking=True)
+                x_ready[i].record(h2d)
+
+        load(0)
+        for i in range(n):
+            if i + 1 < n:
+                load(i + 1)
+            s.wait_event(x_ready[i])
+            if i >= 2:
+                s.wait_event(y_free[i - 2])
+            self.forward(b["x"][i % 2], topk_idx=topk_idx,
+                         topk_gate=topk_gate, y=b["y"][i % 2], stream=s)
+            x_free[i].record(s)
+            y_ready[i].record(s)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(y_ready[i])
+                ys_host[i].copy_(b["y"][i % 2], non_blocking=True)
+                y_free[i].record(d2h)
+        s.wait_stream(d2h)
+        return ys_host
+
     def device_status(self) -> int:
         return int(self.status.item())

@@ -320,3 +320,25 @@ def test_padded_layer_mode_equals_compact_on_kept_pairs():
     for y in (ya, yb):
         err = np.abs(f64(y) - ref["y"]).max() / np.abs(ref["y"]).max()
         assert err <= 1e-2
+
+
+def test_host_stream_matches_forward_bitwise():
+    # forward_host_stream overlaps each batch's copies with its neighbours'
+    # compute; every batch's output must equal forward() on that batch
+    wl = W.WORKLOADS["mixtral_bf16"].with_(T=256, D=512, F=1024)
+    inp = W.make_inputs(wl, device="cpu")
+    layer = MoELayer(wl.T, wl.D, wl.E, wl.k, wl.R, inp["w_r"].to(DEV),
+                     inp["w13"].to(DEV), inp["w2"].to(DEV), F=wl.F,
+                     score=wl.score)
+    g = torch.Generator().manual_seed(3)
+    xs = [torch.randn((wl.T, wl.D), generator=g).to(torch.bfloat16)
+          .pin_memory() for _ in range(5)]
+    ys = [torch.full((wl.T, wl.D), float("nan"),
+                     dtype=torch.bfloat16).pin_memory() for _ in range(5)]
+    layer.forward_host_stream(xs, ys)
+    torch.cuda.synchronize()
+    for xh, yh in zip(xs, ys):
+        ref = layer.forward(xh.to(DEV)).cpu()
+        torch.cuda.synchronize()
+        assert torch.equal(yh, ref)
+    assert layer.device_status() == 0
