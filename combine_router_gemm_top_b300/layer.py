@@ -338,5 +338,44 @@ class MoELayer:
         s.wait_stream(d2h)
         return ys_host
 
+    def capture(self, x, topk_idx=None, topk_gate=None, train=False):
+        """Captures one forward pass on the device input buffer `x` (its
+        storage is reused at every replay) into a CUDA graph and returns a
+        function that replays it.  Every call of the pass is asynchronous,
+        allocates nothing and never synchronises, so the whole layer is one
+        graph launch.  With train=True the training forward and backward
+        are captured instead (the replay takes dy, a device buffer whose
+        storage is reused).  The first, eager pass sets the kernels'
+        shared-memory limits before capture."""
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream())
+        dy = torch.zeros_like(self.y) if train else None
+        with torch.cuda.stream(s):
+            if train:
+                self.forward_train(x, s)
+                self.backward(dy, s)
+            else:
+                self.forward(x, topk_idx, topk_gate, stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        if train:
+            with torch.cuda.graph(graph, stream=s):
+                self.forward_train(x, s)
+                self.backward(dy, s)
+
+            def replay(dy_in):
+                dy.copy_(dy_in)
+                graph.replay()
+                return self._train["dx"]
+            return replay
+        with torch.cuda.graph(graph, stream=s):
+            self.forward(x, topk_idx, topk_gate, stream=s)
+
+        def replay():
+            graph.replay()
+            return self.y
+        return replay
+
     def device_status(self) -> int:
         return int(self.status.item())

@@ -342,3 +342,52 @@ def test_host_stream_matches_forward_bitwise():
         torch.cuda.synchronize()
         assert torch.equal(yh, ref)
     assert layer.device_status() == 0
+
+
+@pytest.mark.parametrize("wl", [
+    W.WORKLOADS["tiny_f32"],
+    W.WORKLOADS["mixtral_bf16"].with_(T=256, D=512, F=1024),
+    W.WORKLOADS["deepseek_bf16"].with_(T=192, D=1024, E=64, F=256),
+], ids=lambda w: w.name)
+def test_graph_replay_matches_eager_bitwise(wl):
+    # the captured pass replays on new data in the same input buffer and
+    # gives exactly what the eager pass gives
+    inp = W.make_inputs(wl, device="cpu")
+    kw = dict(F=wl.F, score=wl.score,
+              sel_bias=None if inp["sel_bias"] is None
+              else inp["sel_bias"].to(DEV),
+              capacity_factor=wl.capacity_factor, n_groups=wl.n_groups,
+              topk_groups=wl.topk_groups,
+              group_score_topk=wl.group_score_topk)
+    layer = MoELayer(wl.T, wl.D, wl.E, wl.k, wl.R, inp["w_r"].to(DEV),
+                     inp["w13"].to(DEV), inp["w2"].to(DEV), **kw)
+    x = inp["x"].to(DEV)
+    replay = layer.capture(x)
+    g = torch.Generator().manual_seed(5)
+    for _ in range(3):
+        new = torch.randn(x.shape, generator=g).to(x.dtype)
+        x.copy_(new.to(DEV))
+        y_graph = replay().clone()
+        y_eager = layer.forward(new.to(DEV)).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(y_graph, y_eager)
+    assert layer.device_status() == 0
+
+
+def test_graph_replay_of_training_step():
+    wl = W.WORKLOADS["mixtral_bf16"].with_(T=256, D=512, F=1024)
+    inp = W.make_inputs(wl, device="cpu")
+    layer = MoELayer(wl.T, wl.D, wl.E, wl.k, wl.R, inp["w_r"].to(DEV),
+                     inp["w13"].to(DEV), inp["w2"].to(DEV), F=wl.F,
+                     score=wl.score)
+    x = inp["x"].to(DEV)
+    replay = layer.capture(x, train=True)
+    g = torch.Generator().manual_seed(9)
+    dy = torch.randn(x.shape, generator=g).to(x.dtype).to(DEV)
+    dx_graph = replay(dy).clone()
+    dw2_graph = layer._train["dw2"].clone()
+    layer.forward_train(x)
+    dx_eager, _, _, dw2_eager = layer.backward(dy)
+    torch.cuda.synchronize()
+    assert torch.equal(dx_graph, dx_eager)
+    assert torch.equal(dw2_graph, dw2_eager)
