@@ -16,6 +16,8 @@
 //                     dx += dlogits W_r (fp32 accumulation, fixed order)
 #include <float.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -346,6 +348,84 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// dW_r for E >= 64 (bf16 x): block = 64 experts x 256 columns over one
+// token slice; thread = 8 experts x 8 columns, 64 accumulators.  16 tokens
+// of x (fp32) and dl sit in shared memory per step; each token costs a
+// thread 4 shared float4 loads for 64 FMAs.
+__global__ void __launch_bounds__(256)
+    dwr_tiled_kernel(int Tn, int E, int D, int t_per_slice,
+                     const float* __restrict__ dl,
+                     const __nv_bfloat16* __restrict__ x,
+                     float* __restrict__ out) {
+  __shared__ __align__(16) float s_x[16][256];
+  __shared__ __align__(16) float s_l[16][64];
+  const int tid = threadIdx.x;
+  const int te = tid >> 5;          // experts e0 + 8*te .. +7
+  const int td = tid & 31;          // columns d0 + 8*td .. +7
+  const int e0 = blockIdx.y * 64;
+  const int d0 = blockIdx.x * 256;
+  const int ts = blockIdx.z * t_per_slice;
+  const int tend = min(Tn, ts + t_per_slice);
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+  for (int t0 = ts; t0 < tend; t0 += 16) {
+    __syncthreads();
+    // 16 tokens x 256 columns: 512 vectors of 8 bf16, two per thread
+    for (int v = tid; v < 512; v += 256) {
+      const int tt = v >> 5, dd = (v & 31) * 8;
+      const int t = t0 + tt, d = d0 + dd;
+      float f[8];
+      if (t < tend && d < D) {
+        Vec16<__nv_bfloat16>::to_f32(
+            ld_nc_v4(x + static_cast<int64_t>(t) * D + d), f);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = 0.0f;
+      }
+      *reinterpret_cast<float4*>(&s_x[tt][dd]) =
+          make_float4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<float4*>(&s_x[tt][dd + 4]) =
+          make_float4(f[4], f[5], f[6], f[7]);
+    }
+    for (int i = tid; i < 16 * 64; i += 256) {
+      const int tt = i >> 6, ee = i & 63;
+      const int t = t0 + tt, e = e0 + ee;
+      s_l[tt][ee] =
+          t < tend && e < E ? dl[static_cast<int64_t>(t) * E + e] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int tt = 0; tt < 16; ++tt) {
+      const float4 l0 = *reinterpret_cast<const float4*>(&s_l[tt][8 * te]);
+      const float4 l1 = *reinterpret_cast<const float4*>(&s_l[tt][8 * te + 4]);
+      const float4 x0 = *reinterpret_cast<const float4*>(&s_x[tt][8 * td]);
+      const float4 x1 = *reinterpret_cast<const float4*>(&s_x[tt][8 * td + 4]);
+      const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+      const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(lv[i], xv[j], acc[i][j]);
+    }
+  }
+  float* o = out + static_cast<int64_t>(blockIdx.z) * E * D;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = e0 + 8 * te + i;
+    const int d = d0 + 8 * td;
+    if (e < E && d < D) {
+      float* p = o + static_cast<int64_t>(e) * D + d;
+      *reinterpret_cast<float4*>(p) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float4*>(p + 4) =
+          make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
+  }
+}
+
 __global__ void dwr_reduce_kernel(int64_t n, int slices,
                                   const float* __restrict__ part,
                                   float* __restrict__ dwr) {
@@ -406,7 +486,7 @@ struct DwrPlan {
 };
 static DwrPlan dwr_plan(int T, int E, int D, int num_sms) {
   DwrPlan p;
-  p.eb = E >= 32 ? 32 : 8;
+  p.eb = E >= 64 ? 64 : (E >= 32 ? 32 : 8);
   const int64_t base = ceil_div(D, 256) * ceil_div(E, p.eb);
   int64_t s = ceil_div(2 * num_sms, base);
   const int64_t max_s = ceil_div(T, 32);
@@ -432,10 +512,21 @@ static void launch_dwr(const DwrPlan& p, int Tn, int E, int D,
   const dim3 g(static_cast<unsigned>(ceil_div(D, 256)),
                static_cast<unsigned>(ceil_div(E, p.eb)),
                static_cast<unsigned>(p.slices));
-  if (p.eb == 32)
-    dwr_kernel<T, 32><<<g, 256, 0, stream>>>(Tn, E, D, p.t_per_slice, dl, x, out);
-  else
-    dwr_kernel<T, 8><<<g, 256, 0, stream>>>(Tn, E, D, p.t_per_slice, dl, x, out);
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    if (p.eb == 64) {
+      dwr_tiled_kernel<<<g, 256, 0, stream>>>(Tn, E, D, p.t_per_slice, dl, x,
+                                              out);
+    } else if (p.eb == 32) {
+      dwr_kernel<T, 32><<<g, 256, 0, stream>>>(Tn, E, D, p.t_per_slice, dl, x, out);
+    } else {
+      dwr_kernel<T, 8><<<g, 256, 0, stream>>>(Tn, E, D, p.t_per_slice, dl, x, out);
+    }
+  } else {
+    if (p.eb >= 32)
+      dwr_kernel<T, 32><<<g, 256, 0, stream>>>(Tn, E, D, p.t_per_slice, dl, x, out);
+    else
+      dwr_kernel<T, 8><<<g, 256, 0, stream>>>(Tn, E, D, p.t_per_slice, dl, x, out);
+  }
   if (p.slices > 1) {
     const int64_t n = static_cast<int64_t>(E) * D;
     dwr_reduce_kernel<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0,

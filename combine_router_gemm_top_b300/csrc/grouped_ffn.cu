@@ -271,6 +271,7 @@ moe_status launch_grouped_ffn_backward(int E, int D, int F, int max_rows,
   g.m_tiles = D / kBM;
   g.n_tiles = static_cast<int>(ceil_div(F, 256));
   g.M = static_cast<int32_t>(ED);
+  g.n_fast = D > F;   // keep the narrower operand (H or dYp) in L2
   g.out = dw2;
   g.out_ld = F;
   g.out_cols = F;
@@ -284,6 +285,7 @@ moe_status launch_grouped_ffn_backward(int E, int D, int F, int max_rows,
   g.m_tiles = 2 * F / kBM;
   g.n_tiles = static_cast<int>(ceil_div(D, 256));
   g.M = static_cast<int32_t>(EF2);
+  g.n_fast = 2 * F > D;   // keep the narrower operand (Xp or [dG|dU]) in L2
   g.out = dw13;
   g.out_ld = D;
   g.out_cols = D;

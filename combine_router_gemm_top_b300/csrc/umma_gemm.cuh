@@ -120,6 +120,8 @@ struct GemmArgs {
   void* out2;               // kUpBwd: H [rows, F]
   int32_t m_total;          // wgrad: output rows per expert (D or 2F)
   int32_t m_tiles;          // wgrad: m_total / 128
+  int32_t n_fast;           // wgrad: column blocks vary fastest (keeps the
+                            // smaller B operand resident in L2)
 };
 
 struct TileInfo {
@@ -167,8 +169,10 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a,
     const int per_e = a.m_tiles * a.n_tiles;
     const int e = t / per_e;
     const int local = t - e * per_e;
-    const int n = local / a.m_tiles;
-    const int m = local - n * a.m_tiles;
+    // tiles running at the same time share the operand that varies
+    // slowest; the other one should be the one that fits L2
+    const int n = a.n_fast ? local % a.n_tiles : local / a.m_tiles;
+    const int m = a.n_fast ? local / a.n_tiles : local - n * a.m_tiles;
     ti.split = 0;
     ti.swap_n = 0;
     ti.a_row = e * a.m_total + m * kBM;   // output row of the tile

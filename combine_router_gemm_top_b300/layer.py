@@ -1,12 +1,21 @@
 """Host-side MoE layer: owns the device buffers of one layer pass and calls
-the five C-ABI entry points in order on one stream.
+the C-ABI entry points in order on one stream.
 
-    route -> dispatch_layout -> permute -> grouped_ffn -> combine
+    forward        route -> dispatch_layout -> permute -> grouped_ffn ->
+                   combine
+    forward_padded the same on the static-capacity [E, C, D] layout
+    forward_train  the forward on the 64-row aligned layout, keeping what
+    + backward     the backward pass needs; then combine, expert, permute
+                   and router backward
+    capture        one step as a CUDA graph
+    forward_host_stream  batches from pinned host memory, copies overlapping
+                   compute
 
 ("Expert Parallelism in LLMs", The Execution Pipeline, steps 1, 2, 4 and 6;
-on one GPU the all-to-all steps 3 and 5 are the identity).  Buffers are
-sized for the worst case (T*k rows) so no step ever waits on the host for
-the dropless row count: expert offsets and kept counts stay on the device.
+on one GPU the all-to-all steps 3 and 5 are the identity; Backward Pass
+Symmetry).  Buffers are sized for the worst case (T*k rows) so no step ever
+waits on the host for the dropless row count: expert offsets and kept
+counts stay on the device.
 """
 from __future__ import annotations
 

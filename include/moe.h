@@ -19,6 +19,8 @@
  * On one GPU the dispatch and combine all-to-alls (steps 3 and 5) are the
  * identity: the expert-contiguous buffer is the send buffer, split by
  * rank_send_counts / rank_send_displs.
+ * Further down: router statistics and the bias step, the dispatch matrix,
+ * the static-capacity layout, and the backward pass of every step.
  *
  * Conventions shared by every call
  *  - Pointers are DEVICE pointers unless marked "host".  The caller owns
