@@ -458,6 +458,7 @@ __global__ void __launch_bounds__(256)
   float acc[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+#pragma unroll 4
   for (int e = 0; e < E; ++e) {
     const float w = static_cast<float>(wr[static_cast<int64_t>(e) * D + d]);
     const float4* q = reinterpret_cast<const float4*>(s_dlt + e * kDxLd);
@@ -488,7 +489,9 @@ static DwrPlan dwr_plan(int T, int E, int D, int num_sms) {
   DwrPlan p;
   p.eb = E >= 64 ? 64 : (E >= 32 ? 32 : 8);
   const int64_t base = ceil_div(D, 256) * ceil_div(E, p.eb);
-  int64_t s = ceil_div(2 * num_sms, base);
+  // the tiled kernel keeps two blocks per SM resident: take as many slices
+  // as fit in one round of them, not one more
+  int64_t s = p.eb == 64 ? (2 * num_sms) / base : ceil_div(2 * num_sms, base);
   const int64_t max_s = ceil_div(T, 32);
   s = s < 1 ? 1 : (s > 64 ? 64 : s);
   s = s > max_s ? max_s : s;
