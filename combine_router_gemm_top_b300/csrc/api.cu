@@ -390,9 +390,9 @@ moe_status moe_permute_backward(int32_t T, int32_t k, int32_t D, int32_t dtype,
 size_t moe_grouped_ffn_backward_workspace_size(int32_t E, int32_t D, int32_t F,
                                                int32_t max_rows,
                                                int32_t dtype) {
-  if (E < 1 || D <= 0 || F <= 0 || max_rows < 0 || dtype != MOE_BF16)
+  if (E < 1 || D <= 0 || F <= 0 || max_rows < 0 || !valid_dtype(dtype))
     return 0;
-  const size_t b = ffn_bwd_ws_bytes(F, max_rows);
+  const size_t b = ffn_bwd_ws_bytes(F, max_rows, dtype);
   return b > 0 ? b : 16;
 }
 
@@ -404,8 +404,25 @@ moe_status moe_grouped_ffn_backward(
     moe_stream_t stream) {
   if (E < 1 || D <= 0 || F <= 0 || max_rows < 0 || !valid_dtype(dtype))
     return MOE_ERR_INVALID;
-  if (dtype != MOE_BF16 || D % 128 != 0 || F % 128 != 0 ||
-      E > kMaxGroupsApi)
+  if (dtype == MOE_F32) {
+    if (xp == nullptr || dyp == nullptr || expert_offsets == nullptr ||
+        w13 == nullptr || w2 == nullptr || dxp == nullptr ||
+        dw13 == nullptr || dw2 == nullptr || workspace == nullptr)
+      return MOE_ERR_INVALID;
+    if (!aligned(workspace, 16) ||
+        workspace_bytes < ffn_bwd_ws_bytes(F, max_rows, dtype))
+      return MOE_ERR_INVALID;
+    if (static_cast<int64_t>(E) * 2 * F * D > INT32_MAX * 64LL)
+      return MOE_ERR_UNSUPPORTED;
+    if (max_rows == 0) return MOE_OK;
+    return launch_grouped_ffn_backward_f32(
+        E, D, F, max_rows, static_cast<const float*>(xp),
+        static_cast<const float*>(dyp), expert_offsets,
+        static_cast<const float*>(w13), static_cast<const float*>(w2),
+        static_cast<float*>(dxp), dw13, dw2, workspace,
+        reinterpret_cast<cudaStream_t>(stream));
+  }
+  if (D % 128 != 0 || F % 128 != 0 || E > kMaxGroupsApi)
     return MOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(E) * 2 * F > INT32_MAX ||
       static_cast<int64_t>(E) * D > INT32_MAX)
@@ -418,7 +435,8 @@ moe_status moe_grouped_ffn_backward(
       !aligned(w2, 256) || !aligned(workspace, 256) || !aligned(dxp, 16) ||
       !aligned(dw13, 16) || !aligned(dw2, 16))
     return MOE_ERR_INVALID;
-  if (workspace_bytes < ffn_bwd_ws_bytes(F, max_rows)) return MOE_ERR_INVALID;
+  if (workspace_bytes < ffn_bwd_ws_bytes(F, max_rows, dtype))
+    return MOE_ERR_INVALID;
   return launch_grouped_ffn_backward(E, D, F, max_rows, xp, dyp,
                                      expert_offsets, w13, w2, dxp, dw13, dw2,
                                      workspace, status,

@@ -184,8 +184,128 @@ namespace moe {
 // ----------------------------------------------------------- backward
 // Workspace of the backward: dH [rows, F], dGU [rows, 2F], H [rows, F]
 // (bf16 each).
-size_t ffn_bwd_ws_bytes(int F, int max_rows) {
-  return static_cast<size_t>(max_rows) * F * 2 * 4;
+size_t ffn_bwd_ws_bytes(int F, int max_rows, int dtype) {
+  return static_cast<size_t>(max_rows) * F * 4 * dtype_bytes(dtype);
+}
+
+// fp32 backward on the CUDA cores: one thread per output element, fp32
+// accumulation in index order (the reference-precision path).
+__global__ void ffn_bwd_dh_f32_kernel(int E, int D, int F, int max_rows,
+                                      const int32_t* __restrict__ off,
+                                      const float* __restrict__ dyp,
+                                      const float* __restrict__ w2,
+                                      float* __restrict__ dh) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int n_rows = min(__ldg(off + E), max_rows);
+  if (i >= static_cast<int64_t>(n_rows) * F) return;
+  const int row = static_cast<int>(i / F);
+  const int f = static_cast<int>(i - static_cast<int64_t>(row) * F);
+  const int e = find_expert(off, E, row);
+  const float* g = dyp + static_cast<int64_t>(row) * D;
+  const float* w = w2 + static_cast<int64_t>(e) * D * F + f;
+  float acc = 0.0f;
+  for (int d = 0; d < D; ++d) acc = fmaf(g[d], w[static_cast<int64_t>(d) * F], acc);
+  dh[i] = acc;
+}
+
+// recomputes gate g and up u, then dG = dH u SiLU'(g), dU = dH SiLU(g) into
+// dgu [rows, 2F] (W13's row order) and H = SiLU(g) u
+__global__ void ffn_bwd_act_f32_kernel(int E, int D, int F, int max_rows,
+                                       const int32_t* __restrict__ off,
+                                       const float* __restrict__ xp,
+                                       const float* __restrict__ w13,
+                                       const float* __restrict__ dh,
+                                       float* __restrict__ dgu,
+                                       float* __restrict__ h) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int n_rows = min(__ldg(off + E), max_rows);
+  if (i >= static_cast<int64_t>(n_rows) * F) return;
+  const int row = static_cast<int>(i / F);
+  const int f = static_cast<int>(i - static_cast<int64_t>(row) * F);
+  const int e = find_expert(off, E, row);
+  const float* x = xp + static_cast<int64_t>(row) * D;
+  const float* w1 = w13 + (static_cast<int64_t>(e) * 2 * F + f) * D;
+  const float* w3 = w1 + static_cast<int64_t>(F) * D;
+  float g = 0.0f, u = 0.0f;
+  for (int d = 0; d < D; ++d) {
+    g = fmaf(x[d], w1[d], g);
+    u = fmaf(x[d], w3[d], u);
+  }
+  const float s = 1.0f / (1.0f + expf(-g));
+  const float d = dh[i];
+  float* o = dgu + static_cast<int64_t>(row) * 2 * F;
+  o[f] = d * u * s * (1.0f + g * (1.0f - s));
+  o[F + f] = d * g * s;
+  h[i] = g * s * u;
+}
+
+__global__ void ffn_bwd_dx_f32_kernel(int E, int D, int F, int max_rows,
+                                      const int32_t* __restrict__ off,
+                                      const float* __restrict__ dgu,
+                                      const float* __restrict__ w13,
+                                      float* __restrict__ dxp) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int n_rows = min(__ldg(off + E), max_rows);
+  if (i >= static_cast<int64_t>(n_rows) * D) return;
+  const int row = static_cast<int>(i / D);
+  const int d = static_cast<int>(i - static_cast<int64_t>(row) * D);
+  const int e = find_expert(off, E, row);
+  const float* g = dgu + static_cast<int64_t>(row) * 2 * F;
+  const float* w = w13 + static_cast<int64_t>(e) * 2 * F * D + d;
+  float acc = 0.0f;
+  for (int f = 0; f < 2 * F; ++f)
+    acc = fmaf(g[f], w[static_cast<int64_t>(f) * D], acc);
+  dxp[i] = acc;
+}
+
+// out[e, m, n] = sum over the rows r of expert e of a[r, m] * b[r, n]
+__global__ void ffn_bwd_wgrad_f32_kernel(int E, int M, int N, int max_rows,
+                                         const int32_t* __restrict__ off,
+                                         const float* __restrict__ a, int lda,
+                                         const float* __restrict__ b, int ldb,
+                                         float* __restrict__ out) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<int64_t>(E) * M * N) return;
+  const int e = static_cast<int>(i / (static_cast<int64_t>(M) * N));
+  const int64_t mn = i - static_cast<int64_t>(e) * M * N;
+  const int m = static_cast<int>(mn / N);
+  const int n = static_cast<int>(mn - static_cast<int64_t>(m) * N);
+  const int r0 = min(__ldg(off + e), max_rows);
+  const int r1 = min(__ldg(off + e + 1), max_rows);
+  float acc = 0.0f;
+  for (int r = r0; r < r1; ++r)
+    acc = fmaf(a[static_cast<int64_t>(r) * lda + m],
+               b[static_cast<int64_t>(r) * ldb + n], acc);
+  out[i] = acc;
+}
+
+moe_status launch_grouped_ffn_backward_f32(int E, int D, int F, int max_rows,
+                                           const float* xp, const float* dyp,
+                                           const int32_t* off,
+                                           const float* w13, const float* w2,
+                                           float* dxp, float* dw13, float* dw2,
+                                           void* ws, cudaStream_t stream) {
+  float* dh = static_cast<float*>(ws);
+  float* dgu = dh + static_cast<size_t>(max_rows) * F;
+  float* h = dgu + static_cast<size_t>(max_rows) * 2 * F;
+  auto grid = [](int64_t n) {
+    return static_cast<unsigned>(ceil_div(n > 0 ? n : 1, 256));
+  };
+  const int64_t rf = static_cast<int64_t>(max_rows) * F;
+  const int64_t rd = static_cast<int64_t>(max_rows) * D;
+  ffn_bwd_dh_f32_kernel<<<grid(rf), 256, 0, stream>>>(E, D, F, max_rows, off,
+                                                      dyp, w2, dh);
+  ffn_bwd_act_f32_kernel<<<grid(rf), 256, 0, stream>>>(E, D, F, max_rows, off,
+                                                       xp, w13, dh, dgu, h);
+  ffn_bwd_dx_f32_kernel<<<grid(rd), 256, 0, stream>>>(E, D, F, max_rows, off,
+                                                      dgu, w13, dxp);
+  const int64_t n2 = static_cast<int64_t>(E) * D * F;
+  ffn_bwd_wgrad_f32_kernel<<<grid(n2), 256, 0, stream>>>(
+      E, D, F, max_rows, off, dyp, D, h, F, dw2);
+  const int64_t n13 = static_cast<int64_t>(E) * 2 * F * D;
+  ffn_bwd_wgrad_f32_kernel<<<grid(n13), 256, 0, stream>>>(
+      E, 2 * F, D, max_rows, off, dgu, 2 * F, xp, D, dw13);
+  return launch_status();
 }
 
 moe_status launch_grouped_ffn_backward(int E, int D, int F, int max_rows,

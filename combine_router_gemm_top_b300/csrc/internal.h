@@ -96,7 +96,13 @@ moe_status launch_pad_fill(int E, int capacity, int D, int dtype,
                            const int32_t* counts, void* buf,
                            cudaStream_t stream, int num_sms);
 
-size_t ffn_bwd_ws_bytes(int F, int max_rows);
+size_t ffn_bwd_ws_bytes(int F, int max_rows, int dtype);
+moe_status launch_grouped_ffn_backward_f32(int E, int D, int F, int max_rows,
+                                           const float* xp, const float* dyp,
+                                           const int32_t* off,
+                                           const float* w13, const float* w2,
+                                           float* dxp, float* dw13, float* dw2,
+                                           void* ws, cudaStream_t stream);
 moe_status launch_grouped_ffn_backward(int E, int D, int F, int max_rows,
                                        const void* xp, const void* dyp,
                                        const int32_t* offsets,

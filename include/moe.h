@@ -423,7 +423,7 @@ MOE_API moe_status moe_permute_backward(int32_t T, int32_t k, int32_t D,
                                         moe_stream_t stream);
 
 /* Bytes of scratch moe_grouped_ffn_backward needs: dH [max_rows, F],
- * dGU [max_rows, 2F] and H [max_rows, F] in bf16. */
+ * dGU [max_rows, 2F] and H [max_rows, F] in the compute dtype. */
 MOE_API size_t moe_grouped_ffn_backward_workspace_size(int32_t E, int32_t D,
                                                        int32_t F,
                                                        int32_t max_rows,
@@ -437,14 +437,15 @@ MOE_API size_t moe_grouped_ffn_backward_workspace_size(int32_t E, int32_t D,
  *     dG   = dH * U * SiLU'(G),  dU = dH * SiLU(G),  H = SiLU(G) * U
  *     dxp  = dG W1_e + dU W3_e                         (dtype out)
  *     dw2[e]  = dyp^T H,  dw13[e] = [dG | dU]^T xp      (fp32 out)
- * An expert with no rows gets zero weight gradients.  All five GEMMs run on
- * the tcgen05 tensor cores (bf16 in, fp32 accumulate).
- *   xp, dyp [max_rows, D] bf16, 256-byte aligned; w13 [E, 2F, D] and
- *   w2 [E, D, F] bf16 (the forward weights); dxp [max_rows, D] bf16 out;
+ * An expert with no rows gets zero weight gradients.  MOE_BF16: all five
+ * GEMMs run on the tcgen05 tensor cores (bf16 in, fp32 accumulate).
+ * MOE_F32: CUDA-core kernels, fp32 throughout, any D and F.
+ *   xp, dyp [max_rows, D] dtype, 256-byte aligned (bf16); w13 [E, 2F, D]
+ *   and w2 [E, D, F] dtype (the forward weights); dxp [max_rows, D] out;
  *   dw13 [E, 2F, D] and dw2 [E, D, F] fp32 out, 16-byte aligned.
- * MOE_BF16 only, D % 128 == 0 and F % 128 == 0 (else MOE_ERR_UNSUPPORTED).
- * Unaligned offsets are detected on the device: MOE_ERR_INVALID in
- * `status` and no weight gradient is written. */
+ * MOE_BF16 needs D % 128 == 0 and F % 128 == 0 (else MOE_ERR_UNSUPPORTED);
+ * there, unaligned offsets are detected on the device: MOE_ERR_INVALID in
+ * `status` and no weight gradient is written.  MOE_F32 takes any offsets. */
 MOE_API moe_status moe_grouped_ffn_backward(
     int32_t E, int32_t D, int32_t F, int32_t max_rows, int32_t dtype,
     const void* xp, const void* dyp, const int32_t* expert_offsets,

@@ -297,3 +297,88 @@ def test_layer_backward_matches_oracle(wl):
                       (dw13, ref["dw13"]), (dw2, ref["dw2"])):
         assert np.isfinite(f64(got)).all()
         assert rel(f64(got), want) <= 2e-2
+
+
+# ------------------------------------------------------ fp32 backward ------
+@pytest.mark.parametrize("counts,D,F", [([10, 0, 37, 64, 1], 64, 96),
+                                        ([130, 70, 5], 40, 128)])
+def test_grouped_ffn_backward_fp32_parity(counts, D, F):
+    # the fp32 path takes any offsets and any D, F; fp32 accumulation over
+    # K <= 256 terms keeps it within 1e-5 of the float64 oracle
+    E = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(off[-1]) + 3
+    g = torch.Generator().manual_seed(D + F)
+    xp = torch.randn((rows, D), generator=g)
+    dyp = torch.randn((rows, D), generator=g)
+    w13 = torch.randn((E, 2 * F, D), generator=g) / math.sqrt(D)
+    w2 = torch.randn((E, D, F), generator=g) / math.sqrt(F)
+    ws = torch.empty(L.moe_grouped_ffn_backward_workspace_size(
+        E, D, F, rows, L.MOE_F32), dtype=torch.uint8, device=DEV)
+    dxp = torch.full((rows, D), float("nan"), device=DEV)
+    dw13 = torch.full((E, 2 * F, D), float("nan"), device=DEV)
+    dw2 = torch.full((E, D, F), float("nan"), device=DEV)
+    st = torch.zeros(1, **I32)
+    L.moe_grouped_ffn_backward(E, D, F, rows, L.MOE_F32, xp.to(DEV),
+                               dyp.to(DEV), torch.tensor(off, device=DEV),
+                               w13.to(DEV), w2.to(DEV), dxp, dw13, dw2, ws, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    X, DY, W13, W2 = f64(xp), f64(dyp), f64(w13), f64(w2)
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b == a:
+            assert (dw13[e] == 0).all() and (dw2[e] == 0).all()
+            continue
+        w1, w3 = O.split_w13(W13[e])
+        dh, dw1, dw3, dw2e = O.expert_backward(X[a:b], w1, w3, W2[e],
+                                               DY[a:b])
+        assert rel(f64(dxp[a:b]), dh) <= 1e-5
+        assert rel(f64(dw13[e, :F]), dw1) <= 1e-5
+        assert rel(f64(dw13[e, F:]), dw3) <= 1e-5
+        assert rel(f64(dw2[e]), dw2e) <= 1e-5
+
+
+@pytest.mark.parametrize("wl", [
+    W.WORKLOADS["tiny_f32"],
+    W.WORKLOADS["deepseek_bf16"].with_(name="deepseek_f32_small", T=96, D=64,
+                                       E=32, F=48, dtype="f32"),
+    W.WORKLOADS["switch_bf16"].with_(name="switch_f32_small", T=512, D=32,
+                                     E=16, F=64, dtype="f32"),
+], ids=lambda w: w.name)
+def test_layer_backward_fp32_tight(wl):
+    # the whole fp32 training step against the float64 oracle at the fp32
+    # bar: combine, expert, permute and router backward all in fp32
+    inp = W.make_inputs(wl, device="cpu")
+    layer = MoELayer(wl.T, wl.D, wl.E, wl.k, wl.R, inp["w_r"].to(DEV),
+                     inp["w13"].to(DEV), inp["w2"].to(DEV), F=wl.F,
+                     score=wl.score,
+                     sel_bias=None if inp["sel_bias"] is None
+                     else inp["sel_bias"].to(DEV),
+                     logit_offset=None if inp["logit_offset"] is None
+                     else inp["logit_offset"].to(DEV),
+                     capacity_factor=wl.capacity_factor, n_groups=wl.n_groups,
+                     topk_groups=wl.topk_groups,
+                     group_score_topk=wl.group_score_topk, keep_logits=True)
+    x = inp["x"].to(DEV)
+    y = layer.forward_train(x).clone()
+    g = torch.Generator().manual_seed(wl.T + 1)
+    dy = torch.randn((wl.T, wl.D), generator=g)
+    dx, dw_r, dw13, dw2 = layer.backward(dy.to(DEV))
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    cap = O.expert_capacity(wl.capacity_factor, wl.T, wl.k, wl.E)
+    ref = O.moe_backward(
+        f64(inp["x"]), f64(inp["w_r"]), f64(dy), wl.k, wl.E, wl.R, wl.score,
+        w13=f64(inp["w13"]), w2=f64(inp["w2"]),
+        sel_bias=None if inp["sel_bias"] is None else inp["sel_bias"].numpy(),
+        logit_offset=None if inp["logit_offset"] is None
+        else inp["logit_offset"].numpy(),
+        n_groups=wl.n_groups, topk_groups=wl.topk_groups,
+        group_score_topk=wl.group_score_topk, capacity=cap,
+        logits=layer.logits.cpu().numpy())
+    assert (i64(layer.topk_idx) == ref["forward"]["topk_idx"]).all()
+    assert rel(f64(y), ref["forward"]["y"]) <= 1e-5
+    for got, want in ((dx, ref["dx"]), (dw_r, ref["dw_r"]),
+                      (dw13, ref["dw13"]), (dw2, ref["dw2"])):
+        assert rel(f64(got), want) <= 1e-5
