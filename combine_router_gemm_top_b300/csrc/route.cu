@@ -49,26 +49,15 @@ __device__ __forceinline__ float sigmoid_key_f32(float l) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
 }
 
-struct KeyIdx {
-  float key;
-  int idx;
-};
-// a beats b: larger key, or equal key and lower index
-__device__ __forceinline__ bool beats(float ka, int ia, float kb, int ib) {
-  return ka > kb || (ka == kb && ia < ib);
+// Order-preserving code of an fp32 selection key: for keys a, b (+0 and -0
+// equal), a > b exactly when key_code(a) > key_code(b).  Every key, even
+// -inf, codes above 0, and 0 marks an expert that is not (or no longer)
+// eligible.
+__device__ __forceinline__ uint32_t key_code(float f) {
+  const uint32_t u = f == 0.0f ? 0u : __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-__device__ __forceinline__ KeyIdx warp_best(KeyIdx v) {
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) {
-    const float ok = __shfl_xor_sync(0xffffffffu, v.key, d);
-    const int oi = __shfl_xor_sync(0xffffffffu, v.idx, d);
-    if (beats(ok, oi, v.key, v.idx)) {
-      v.key = ok;
-      v.idx = oi;
-    }
-  }
-  return v;
-}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
@@ -81,79 +70,159 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// The winner among the warp's candidates: lane l holds expert l + 32*i in
+// code[i].  Largest code first, the lower expert index on equal codes; -1
+// when no candidate is eligible.  Two warp reductions (redux.sync) per call.
+template <int NI>
+__device__ __forceinline__ int warp_argmax(const uint32_t (&code)[NI],
+                                           int lane) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) m = max(m, code[i]);
+  const uint32_t top = __reduce_max_sync(0xffffffffu, m);
+  if (top == 0) return -1;
+  uint32_t first = 0xffffffffu;
+#pragma unroll
+  for (int i = NI - 1; i >= 0; --i)
+    if (code[i] == top) first = static_cast<uint32_t>(lane + 32 * i);
+  return static_cast<int>(__reduce_min_sync(0xffffffffu, first));
+}
+
+// group of expert e (< 256) for group size gs: e / gs through one fp32
+// multiply.  (e + 0.5) / gs lies at least 1/512 away from an integer and the
+// product's error is below 2^-15, so truncation gives the exact quotient.
+__device__ __forceinline__ int group_of(int e, float inv_gs) {
+  return static_cast<int>((static_cast<float>(e) + 0.5f) * inv_gs);
+}
+
+constexpr int kSelWarps = 8;
+constexpr int kSelGroupTop = 8;   // per-lane scan handles group_score_topk <= 8
+
 // One warp per token; lane l holds experts e = l + 32*i, i < NI.
 template <int NI>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kSelWarps * 32)
     route_select_kernel(RouteSelectArgs a) {
-  const int warps = blockDim.x >> 5;
+  // keys of each warp's token for the group scan, one pad word per 32 so
+  // that lanes reading along different groups hit different banks
+  __shared__ float skey[kSelWarps][256 + 8];
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5);
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kSelWarps + warp;
   if (t >= a.T) return;
   const int E = a.E;
 
-  float lg[NI], key[NI];
-  bool elig[NI];
+  // split-K partial sums added in split order; the loads of one split are
+  // independent of each other
+  float lg[NI];
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int e = lane + 32 * i;
-    elig[i] = e < E;
-    float l = 0.0f;
-    if (elig[i]) {
-      // split-K partial sums added in split order
-      l = a.partial[t * E + e];
-      for (int s = 1; s < a.splits; ++s)
-        l = __fadd_rn(l, a.partial[(static_cast<int64_t>(s) * a.T + t) * E + e]);
-      if (a.logit_offset != nullptr) l = __fadd_rn(l, a.logit_offset[e]);
-      if (a.logits_out != nullptr) a.logits_out[t * E + e] = l;
+    lg[i] = e < E ? a.partial[t * E + e] : 0.0f;
+  }
+#pragma unroll 2
+  for (int s = 1; s < a.splits; ++s) {
+    const float* ps = a.partial + (static_cast<int64_t>(s) * a.T + t) * E;
+    float p[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int e = lane + 32 * i;
+      p[i] = e < E ? ps[e] : 0.0f;
     }
-    lg[i] = l;
-    float k = l;
-    if (a.score == MOE_SCORE_SIGMOID_BIAS && elig[i]) {
-      k = sigmoid_key_f32(l);
-      if (a.sel_bias != nullptr) k = __fadd_rn(k, a.sel_bias[e]);
-    }
-    key[i] = k;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) lg[i] = __fadd_rn(lg[i], p[i]);
   }
 
-  // group-limited selection: keep the topk_groups best groups
+  float key[NI];
+  uint32_t code[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      if (a.logit_offset != nullptr) lg[i] = __fadd_rn(lg[i], a.logit_offset[e]);
+      if (a.logits_out != nullptr) a.logits_out[t * E + e] = lg[i];
+      float k = lg[i];
+      if (a.score == MOE_SCORE_SIGMOID_BIAS) {
+        k = sigmoid_key_f32(k);
+        if (a.sel_bias != nullptr) k = __fadd_rn(k, a.sel_bias[e]);
+      }
+      key[i] = k;
+      code[i] = key_code(k);
+    } else {
+      key[i] = 0.0f;
+      code[i] = 0;
+    }
+  }
+
+  // group-limited selection: score each group by the sum of its
+  // group_score_topk largest keys (added largest first), keep the
+  // topk_groups best groups (lower group index on equal scores)
   if (a.n_groups > 1) {
     const int gs = E / a.n_groups;
-    float my_gscore = -FLT_MAX;   // lane g holds group g's score
-    for (int g = 0; g < a.n_groups; ++g) {
-      uint32_t taken = 0;        // per-lane bitmask over its NI slots
-      float acc = 0.0f;
-      for (int j = 0; j < a.group_score_topk; ++j) {
-        KeyIdx best{-INFINITY, 0x7fffffff};
+    const float inv_gs = 1.0f / static_cast<float>(gs);
+    const int m = a.group_score_topk;
+    float gscore = 0.0f;   // lane g < n_groups: group g's score
+    if (m <= kSelGroupTop) {
+      // lane g scans its group's keys, keeping the m largest in a sorted
+      // list; equal keys are interchangeable for the sum
+      float* sk = skey[warp];
 #pragma unroll
-        for (int i = 0; i < NI; ++i) {
-          const int e = lane + 32 * i;
-          if (elig[i] && e / gs == g && !((taken >> i) & 1u) &&
-              beats(key[i], e, best.key, best.idx)) {
-            best.key = key[i];
-            best.idx = e;
+      for (int i = 0; i < NI; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) sk[e + (e >> 5)] = key[i];
+      }
+      __syncwarp();
+      if (lane < a.n_groups) {
+        float v[kSelGroupTop];
+#pragma unroll
+        for (int j = 0; j < kSelGroupTop; ++j) v[j] = -INFINITY;
+        for (int e = lane * gs; e < (lane + 1) * gs; ++e) {
+          float x = sk[e + (e >> 5)];
+#pragma unroll
+          for (int j = 0; j < kSelGroupTop; ++j) {
+            const float hi = fmaxf(v[j], x);
+            x = fminf(v[j], x);
+            v[j] = hi;
           }
         }
-        best = warp_best(best);
-        acc = __fadd_rn(acc, best.key);
+#pragma unroll
+        for (int j = 0; j < kSelGroupTop; ++j)
+          if (j < m) gscore = __fadd_rn(gscore, v[j]);
+      }
+    } else {
+      // larger m: m warp-wide arg-max rounds per group
+      for (int g = 0; g < a.n_groups; ++g) {
+        uint32_t c[NI];
 #pragma unroll
         for (int i = 0; i < NI; ++i)
-          if (lane + 32 * i == best.idx) taken |= 1u << i;
+          c[i] = group_of(lane + 32 * i, inv_gs) == g ? code[i] : 0u;
+        float acc = 0.0f;   // the same on every lane, largest key first
+        for (int j = 0; j < m; ++j) {
+          const int w = warp_argmax<NI>(c, lane);
+          float mine = 0.0f;
+#pragma unroll
+          for (int i = 0; i < NI; ++i) {
+            if (lane + 32 * i == w) {
+              mine = key[i];
+              c[i] = 0u;
+            }
+          }
+          acc = __fadd_rn(acc, __shfl_sync(0xffffffffu, mine, w & 31));
+        }
+        if (lane == g) gscore = acc;
       }
-      if (lane == g) my_gscore = acc;
     }
+    uint32_t gc[1] = {lane < a.n_groups ? key_code(gscore) : 0u};
     uint32_t chosen = 0;
-    bool gtaken = false;
     for (int j = 0; j < a.topk_groups; ++j) {
-      KeyIdx c{(lane < a.n_groups && !gtaken) ? my_gscore : -INFINITY,
-               (lane < a.n_groups && !gtaken) ? lane : 0x7fffffff};
-      c = warp_best(c);
-      chosen |= 1u << c.idx;
-      if (lane == c.idx) gtaken = true;
+      const int w = warp_argmax<1>(gc, lane);
+      if (w < 0) break;
+      chosen |= 1u << w;
+      if (lane == w) gc[0] = 0u;
     }
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
       const int e = lane + 32 * i;
-      if (elig[i] && !((chosen >> (e / gs)) & 1u)) elig[i] = false;
+      if (e < E && !((chosen >> group_of(e, inv_gs)) & 1u)) code[i] = 0u;
     }
   }
 
@@ -161,52 +230,44 @@ __global__ void __launch_bounds__(256)
   int my_idx = -1;
   float my_logit = 0.0f;
   for (int j = 0; j < a.k; ++j) {
-    KeyIdx best{-INFINITY, 0x7fffffff};
-    float best_l = 0.0f;
+    const int w = warp_argmax<NI>(code, lane);
+    float mine = 0.0f;
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-      const int e = lane + 32 * i;
-      if (elig[i] && beats(key[i], e, best.key, best.idx)) {
-        best.key = key[i];
-        best.idx = e;
-        best_l = lg[i];
+      if (lane + 32 * i == w) {
+        mine = lg[i];
+        code[i] = 0u;
       }
     }
-    const KeyIdx w = warp_best(best);
-    // the owner lane of the winner broadcasts its logit
-    const int owner = w.idx & 31;
-    const float wl = __shfl_sync(0xffffffffu, best_l, owner);
+    const float wl = __shfl_sync(0xffffffffu, mine, w & 31);
     if (lane == j) {
-      my_idx = w.idx;
+      my_idx = w;
       my_logit = wl;
     }
-#pragma unroll
-    for (int i = 0; i < NI; ++i)
-      if (lane + 32 * i == w.idx) elig[i] = false;
   }
 
   // gates
   const bool slot = lane < a.k;
   float g = 0.0f;
   if (a.score == MOE_SCORE_SOFTMAX_TOPK) {
-    const float m = __shfl_sync(0xffffffffu, my_logit, 0);   // slot 0 = max
-    const float ex = slot ? expf(my_logit - m) : 0.0f;
+    const float mx = __shfl_sync(0xffffffffu, my_logit, 0);   // slot 0 = max
+    const float ex = slot ? expf(my_logit - mx) : 0.0f;
     g = ex / warp_sum(ex);
   } else if (a.score == MOE_SCORE_SOFTMAX_FULL) {
-    float m = -FLT_MAX;
+    float mx = -FLT_MAX;
 #pragma unroll
     for (int i = 0; i < NI; ++i)
-      if (lane + 32 * i < E) m = fmaxf(m, lg[i]);
-    m = warp_max(m);
+      if (lane + 32 * i < E) mx = fmaxf(mx, lg[i]);
+    mx = warp_max(mx);
     float z = 0.0f;
 #pragma unroll
     for (int i = 0; i < NI; ++i)
-      if (lane + 32 * i < E) z += expf(lg[i] - m);
+      if (lane + 32 * i < E) z += expf(lg[i] - mx);
     z = warp_sum(z);
-    g = slot ? expf(my_logit - m) / z : 0.0f;
+    g = slot ? expf(my_logit - mx) / z : 0.0f;
   } else {
-    const float s = slot ? sigmoid_key_f32(my_logit) : 0.0f;
-    g = s / warp_sum(s);
+    const float sg = slot ? sigmoid_key_f32(my_logit) : 0.0f;
+    g = sg / warp_sum(sg);
   }
   if (slot) {
     a.topk_idx[t * a.k + lane] = my_idx;
@@ -328,7 +389,7 @@ moe_status launch_route(const moe_route_cfg& c, const void* x, const void* w_r,
   s.topk_idx = topk_idx;
   s.topk_gate = topk_gate;
   s.logits_out = logits_out;
-  const int warps = 8;
+  const int warps = kSelWarps;
   const unsigned grid = static_cast<unsigned>(ceil_div(c.T, warps));
   const int ni = static_cast<int>(ceil_div(c.E, 32));
   if (ni <= 1)

@@ -223,6 +223,13 @@ ROUTE_CASES = [
     (64, 128, 4, 4, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
     (1, 64, 8, 1, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
     (513, 96, 24, 5, torch.float32, "sigmoid_bias", (3, 2, 2), None, None, 0.05),
+    # group scores over more than 8 keys (the warp-round path)
+    (333, 128, 64, 6, torch.bfloat16, "sigmoid_bias", (4, 2, 12), None, None, 0.2),
+    (300, 128, 96, 8, torch.bfloat16, "softmax_topk", (6, 3, 16), None, None, None),
+    # 32 groups of 8, every lane scoring one group
+    (400, 256, 256, 8, torch.bfloat16, "sigmoid_bias", (32, 6, 2), None, None, 0.1),
+    # E not a multiple of 32, groups straddling lanes
+    (211, 128, 200, 7, torch.bfloat16, "sigmoid_bias", (8, 3, 5), None, None, 0.1),
 ]
 
 
@@ -246,6 +253,22 @@ def test_route_ties_go_to_lower_index():
     idx, gate, logits = run_route(x, w, None, None, k, "softmax_topk")
     assert (logits == xl).all()
     ridx, rgate = O.route_from_logits(xl, k, "softmax_topk")
+    assert (idx == ridx).all()
+    assert np.abs(gate - rgate).max() <= 2e-6
+
+
+@pytest.mark.parametrize("groups", [(8, 3, 2), (4, 2, 8), (2, 1, 12)])
+def test_route_group_ties_go_to_lower_index(groups):
+    # integer logits: equal keys and equal group scores everywhere; the lower
+    # group and the lower expert must win every tie
+    T, E, k = 640, 32, 5
+    rng = np.random.default_rng(11)
+    xl = rng.integers(-2, 3, size=(T, E)).astype(np.float32)
+    x = torch.tensor(xl).to(torch.bfloat16)
+    w = torch.eye(E).to(torch.bfloat16)
+    idx, gate, logits = run_route(x, w, None, None, k, "softmax_topk", groups)
+    assert (logits == xl).all()
+    ridx, rgate = O.route_from_logits(xl, k, "softmax_topk", None, *groups)
     assert (idx == ridx).all()
     assert np.abs(gate - rgate).max() <= 2e-6
 
