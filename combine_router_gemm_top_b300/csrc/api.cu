@@ -446,7 +446,8 @@ moe_status moe_grouped_ffn_backward(
 
 size_t moe_route_backward_workspace_size(const moe_route_cfg* cfg) {
   if (!route_cfg_ok(cfg)) return 0;
-  const size_t b = route_bwd_ws_bytes(cfg->T, cfg->D, cfg->E, num_sms());
+  const size_t b =
+      route_bwd_ws_bytes(cfg->T, cfg->D, cfg->E, cfg->dtype, num_sms());
   return b > 0 ? b : 16;
 }
 
@@ -456,7 +457,6 @@ moe_status moe_route_backward(const moe_route_cfg* cfg, const void* x,
                               float* dlogits, float* dw_r, void* dx,
                               void* workspace, size_t workspace_bytes,
                               int32_t* status, moe_stream_t stream) {
-  (void)status;
   if (!route_cfg_ok(cfg)) return MOE_ERR_INVALID;
   if (cfg->T == 0) return MOE_OK;
   if (logits == nullptr || topk_idx == nullptr || dgate == nullptr ||
@@ -464,15 +464,22 @@ moe_status moe_route_backward(const moe_route_cfg* cfg, const void* x,
     return MOE_ERR_INVALID;
   if (dw_r != nullptr && x == nullptr) return MOE_ERR_INVALID;
   if (dx != nullptr && w_r == nullptr) return MOE_ERR_INVALID;
+  if (route_bwd_tensor(cfg->dtype, cfg->E, cfg->D) &&
+      ((dw_r != nullptr && !aligned(x, 16)) ||
+       (dx != nullptr && (!aligned(dx, 16) || !aligned(w_r, 16)))))
+    return MOE_ERR_INVALID;
   const int sms = num_sms();
-  const size_t need = route_bwd_ws_bytes(cfg->T, cfg->D, cfg->E, sms);
-  if (dw_r != nullptr && need > 0 &&
+  const size_t need =
+      route_bwd_ws_bytes(cfg->T, cfg->D, cfg->E, cfg->dtype, sms);
+  if (route_bwd_uses_ws(cfg->dtype, cfg->E, cfg->D, dw_r != nullptr,
+                        dx != nullptr) &&
+      need > 0 &&
       (workspace == nullptr || workspace_bytes < need ||
        !aligned(workspace, 16)))
     return MOE_ERR_INVALID;
   return launch_route_backward(cfg->T, cfg->D, cfg->E, cfg->k, cfg->score,
                                cfg->dtype, x, w_r, logits, topk_idx, dgate,
-                               dlogits, dw_r, dx, workspace,
+                               dlogits, dw_r, dx, workspace, status,
                                reinterpret_cast<cudaStream_t>(stream), sms);
 }
 

@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "umma_gemm.cuh"
 
 namespace moe {
 
@@ -220,7 +221,8 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
                    const float* __restrict__ logits,
                    const int32_t* __restrict__ topk_idx,
                    const float* __restrict__ dgate,
-                   float* __restrict__ dlogits) {
+                   float* __restrict__ dlogits,
+                   __nv_bfloat16* __restrict__ dl2) {
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kBwdWarps + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -302,7 +304,18 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int e = lane + 32 * i;
-    if (e < E) dlogits[t * E + e] = out[i];
+    if (e < E) {
+      dlogits[t * E + e] = out[i];
+      if (dl2 != nullptr) {
+        // two bf16 terms: hi = bf16(dl), lo = bf16(dl - hi) (the difference
+        // is exact in fp32)
+        const __nv_bfloat16 hi = __float2bfloat16_rn(out[i]);
+        const __nv_bfloat16 lo =
+            __float2bfloat16_rn(out[i] - __bfloat162float(hi));
+        dl2[t * 2 * E + e] = hi;
+        dl2[t * 2 * E + E + e] = lo;
+      }
+    }
   }
 }
 
@@ -501,10 +514,118 @@ static DwrPlan dwr_plan(int T, int E, int D, int num_sms) {
   return p;
 }
 
-size_t route_bwd_ws_bytes(int T, int D, int E, int num_sms) {
+// Tensor-core router backward: bf16, E and D multiples of 64 (whole
+// 64-wide boxes of dL2 and W_r, whole 32-column epilogue chunks).
+bool route_bwd_tensor(int dtype, int E, int D) {
+  return dtype == MOE_BF16 && E % 64 == 0 && D % 64 == 0;
+}
+
+struct RbwdPlan {
+  int k_blocks;      // dW_r contraction blocks: hi and lo of each 64 tokens
+  int splits, kb_per_split;
+  size_t dl2_bytes;  // dL2 [T, 2E] bf16, rounded up to 256 bytes
+};
+static RbwdPlan rbwd_plan(int T, int E, int D, int num_sms) {
+  RbwdPlan p;
+  p.k_blocks = static_cast<int>(2 * ceil_div(T, kBK));
+  const int64_t base = ceil_div(E, kBM) * ceil_div(D, 256);
+  // fewest rounds of K blocks on the busiest SM; at most 8 splits so the
+  // fp32 partials stay small
+  int64_t best = INT64_MAX;
+  p.kb_per_split = p.k_blocks;
+  for (int s = 1; s <= 8; ++s) {
+    const int kbps = static_cast<int>(ceil_div(p.k_blocks, s));
+    const int64_t real_s = ceil_div(p.k_blocks, kbps);
+    const int64_t cost = ceil_div(base * real_s, num_sms) * kbps;
+    if (cost < best) {
+      best = cost;
+      p.kb_per_split = kbps;
+    }
+  }
+  p.splits = static_cast<int>(ceil_div(p.k_blocks, p.kb_per_split));
+  p.dl2_bytes = (static_cast<size_t>(T) * 2 * E * 2 + 255) & ~size_t(255);
+  return p;
+}
+
+size_t route_bwd_ws_bytes(int T, int D, int E, int dtype, int num_sms) {
+  if (route_bwd_tensor(dtype, E, D)) {
+    const RbwdPlan p = rbwd_plan(T, E, D, num_sms);
+    return p.dl2_bytes + (p.splits > 1 ? static_cast<size_t>(p.splits) * E *
+                                             D * sizeof(float)
+                                       : 0);
+  }
   const DwrPlan p = dwr_plan(T, E, D, num_sms);
   return p.slices > 1 ? static_cast<size_t>(p.slices) * E * D * sizeof(float)
                       : 0;
+}
+
+bool route_bwd_uses_ws(int dtype, int E, int D, bool dw_r, bool dx) {
+  return route_bwd_tensor(dtype, E, D) ? (dw_r || dx) : dw_r;
+}
+
+// dx += dL2 . [W_r; W_r] and dW_r = [hi; lo]^T . [x; x] on the tensor cores.
+static moe_status launch_route_backward_tc(int T, int D, int E,
+                                           const __nv_bfloat16* x,
+                                           const __nv_bfloat16* w_r,
+                                           const __nv_bfloat16* dl2,
+                                           float* dw_r, __nv_bfloat16* dx,
+                                           float* part, int32_t* status,
+                                           cudaStream_t stream, int num_sms) {
+  if (dx != nullptr) {
+    CUtensorMap tm_dl, tm_w;
+    if (!make_tmap_bf16_2d(&tm_dl, dl2, 2 * E, T, kBM) ||
+        !make_tmap_bf16_2d(&tm_w, w_r, D, E, 64))
+      return MOE_ERR_CUDA;
+    GemmArgs g{};
+    g.M = T;
+    g.k_blocks = 2 * E / kBK;
+    g.kb_per_split = g.k_blocks;
+    g.splits = 1;
+    g.BN = 256;
+    g.stages = 4;
+    g.tmem_cols = 512;
+    g.E = E;
+    g.n_tiles = static_cast<int>(ceil_div(D, 256));
+    g.out = dx;
+    g.out_ld = D;
+    g.out_cols = D;
+    g.status = status;
+    g.wait_limit_ns = kWaitLimitNs;
+    const moe_status st = launch_umma<kRDX>(tm_dl, tm_w, g, stream, num_sms);
+    if (st != MOE_OK) return st;
+  }
+  if (dw_r != nullptr) {
+    const RbwdPlan p = rbwd_plan(T, E, D, num_sms);
+    CUtensorMap tm_dl, tm_x;
+    if (!make_tmap_bf16_2d(&tm_dl, dl2, 2 * E, T, 64) ||
+        !make_tmap_bf16_2d(&tm_x, x, D, T, 64))
+      return MOE_ERR_CUDA;
+    GemmArgs g{};
+    g.M = E;
+    g.k_blocks = p.k_blocks;
+    g.kb_per_split = p.kb_per_split;
+    g.splits = p.splits;
+    g.BN = 256;
+    g.stages = 3;
+    g.tmem_cols = 512;
+    g.E = E;
+    g.n_tiles = static_cast<int>(ceil_div(D, 256));
+    g.out = p.splits > 1 ? part : dw_r;
+    g.out_ld = D;
+    g.out_cols = D;
+    g.row_limit = E;
+    g.split_stride = static_cast<int64_t>(E) * D;
+    g.status = status;
+    g.wait_limit_ns = kWaitLimitNs;
+    const moe_status st = launch_umma<kRDW>(tm_dl, tm_x, g, stream, num_sms);
+    if (st != MOE_OK) return st;
+    if (p.splits > 1) {
+      const int64_t n = static_cast<int64_t>(E) * D;
+      dwr_reduce_kernel<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0,
+                          stream>>>(n, p.splits, part, dw_r);
+    }
+  }
+  return launch_status();
 }
 
 template <typename T>
@@ -542,18 +663,31 @@ moe_status launch_route_backward(int T, int D, int E, int k, int score,
                                  const float* logits, const int32_t* topk_idx,
                                  const float* dgate, float* dlogits,
                                  float* dw_r, void* dx, void* ws,
-                                 cudaStream_t stream, int num_sms) {
+                                 int32_t* status, cudaStream_t stream,
+                                 int num_sms) {
   if (T == 0) return MOE_OK;
+  const bool tc = route_bwd_tensor(dtype, E, D) &&
+                  (dw_r != nullptr || dx != nullptr);
+  __nv_bfloat16* dl2 = tc ? static_cast<__nv_bfloat16*>(ws) : nullptr;
   const unsigned g1 = static_cast<unsigned>(ceil_div(T, kBwdWarps));
   const int ni = static_cast<int>(ceil_div(E, 32));
   if (ni <= 1)
-    dlogits_kernel<1><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits);
+    dlogits_kernel<1><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits, dl2);
   else if (ni <= 2)
-    dlogits_kernel<2><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits);
+    dlogits_kernel<2><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits, dl2);
   else if (ni <= 4)
-    dlogits_kernel<4><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits);
+    dlogits_kernel<4><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits, dl2);
   else
-    dlogits_kernel<8><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits);
+    dlogits_kernel<8><<<g1, kBwdWarps * 32, 0, stream>>>(T, E, k, score, logits, topk_idx, dgate, dlogits, dl2);
+  if (tc) {
+    const RbwdPlan p = rbwd_plan(T, E, D, num_sms);
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                           p.dl2_bytes);
+    return launch_route_backward_tc(
+        T, D, E, static_cast<const __nv_bfloat16*>(x),
+        static_cast<const __nv_bfloat16*>(w_r), dl2, dw_r,
+        static_cast<__nv_bfloat16*>(dx), part, status, stream, num_sms);
+  }
   const DwrPlan p = dwr_plan(T, E, D, num_sms);
   const dim3 gx(static_cast<unsigned>(ceil_div(D, 256)),
                 static_cast<unsigned>(ceil_div(T, 32)));

@@ -77,24 +77,6 @@ size_t ffn_ws_bytes(int E, int D, int F, int max_rows, int dtype) {
   return static_cast<size_t>(max_rows) * F * dtype_bytes(dtype);
 }
 
-template <int MODE>
-static moe_status launch_umma(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                              const GemmArgs& g, cudaStream_t stream,
-                              int num_sms) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(umma_gemm_kernel<MODE>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             227 * 1024) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
-  }
-  const size_t smem =
-      umma_gemm_smem_bytes(g.BN, g.stages, ModeInfo<MODE>::wgrad);
-  umma_gemm_kernel<MODE><<<num_sms, kGemmThreads, smem, stream>>>(tmA, tmB, g);
-  return launch_status();
-}
-
 moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
                               const void* xp, const int32_t* offsets,
                               const void* w13, const void* w2, void* yp,

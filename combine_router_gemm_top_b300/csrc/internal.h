@@ -125,13 +125,16 @@ moe_status launch_aligned_layout(int T, int k, int E, int align,
 moe_status launch_aligned_fill(int E, int D, int dtype, const int32_t* offsets,
                                const int32_t* offsets_aligned, void* buf,
                                cudaStream_t stream);
-size_t route_bwd_ws_bytes(int T, int D, int E, int num_sms);
+size_t route_bwd_ws_bytes(int T, int D, int E, int dtype, int num_sms);
+bool route_bwd_tensor(int dtype, int E, int D);
+bool route_bwd_uses_ws(int dtype, int E, int D, bool dw_r, bool dx);
 moe_status launch_route_backward(int T, int D, int E, int k, int score,
                                  int dtype, const void* x, const void* w_r,
                                  const float* logits, const int32_t* topk_idx,
                                  const float* dgate, float* dlogits,
                                  float* dw_r, void* dx, void* ws,
-                                 cudaStream_t stream, int num_sms);
+                                 int32_t* status, cudaStream_t stream,
+                                 int num_sms);
 
 moe_status launch_sigmoid_key(const float* l, float* out, int n,
                               cudaStream_t stream);

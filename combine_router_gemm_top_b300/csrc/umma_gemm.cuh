@@ -40,6 +40,17 @@
 //           expert's token rows (the contraction), tile = (expert, 128
 //           output rows, 256 output columns), fp32 out.  An expert with no
 //           rows gets zeros.
+// Router backward modes.  The fp32 logit gradient enters as two bf16 terms
+// dl = hi + lo (hi = bf16(dl), lo = bf16(dl - hi)), stored side by side as
+// dL2 [T, 2E]; each product with a bf16 operand is exact in the fp32
+// accumulator, so the split carries dl to about 2^-17 relative.
+//   kRDX    dx[t, :] += dL2[t, :] . [W_r; W_r]: A = dL2 rows (K = 2E,
+//           K-major), B = W_r [E, D] read MN-major (K row = k mod E);
+//           the epilogue adds into the bf16 dx in place.
+//   kRDW    dW_r = [hi; lo]^T . [x; x]: A = dL2 read MN-major (expert
+//           columns), B = x read MN-major, K = 2T with the hi and lo halves
+//           of each 64-token block adjacent; split-K tiles write fp32
+//           partials [split][E][D].
 // Ragged tails (grouped modes): the last row block of an expert with at most
 // 112 rows runs with the operands swapped.  The same shared-memory tiles
 // feed two MMAs of shape 128 x n x 16, n = the tail rounded up to 16: the
@@ -63,7 +74,8 @@ namespace moe {
 
 enum GemmMode {
   kRoute = 0, kUp = 1, kDown = 2,
-  kDH = 3, kUpBwd = 4, kDX = 5, kWG2 = 6, kWG13 = 7
+  kDH = 3, kUpBwd = 4, kDX = 5, kWG2 = 6, kWG13 = 7,
+  kRDX = 8, kRDW = 9
 };
 
 // Static properties of a mode.
@@ -75,8 +87,11 @@ struct ModeInfo {
                                     MODE == kDX;
   // per-expert weight gradient: M x N output, K = the expert's token rows
   static constexpr bool wgrad = MODE == kWG2 || MODE == kWG13;
-  static constexpr bool a_mn = wgrad;
-  static constexpr bool b_mn = MODE == kDH || MODE == kDX || wgrad;
+  static constexpr bool a_mn = wgrad || MODE == kRDW;
+  static constexpr bool b_mn = MODE == kDH || MODE == kDX || wgrad ||
+                               MODE == kRDX || MODE == kRDW;
+  // fp32 output through the per-warp staging tiles
+  static constexpr bool staged = wgrad || MODE == kRDW;
   static constexpr bool swap_tails = MODE == kUp || MODE == kDown;
   // B tile is gate rows stacked on up rows
   static constexpr bool gate_up = MODE == kUp || MODE == kUpBwd;
@@ -122,6 +137,9 @@ struct GemmArgs {
   int32_t m_tiles;          // wgrad: m_total / 128
   int32_t n_fast;           // wgrad: column blocks vary fastest (keeps the
                             // smaller B operand resident in L2)
+  // router backward
+  int32_t row_limit;        // kRDW: output rows (E); 0 = no row mask
+  int64_t split_stride;     // kRDW: elements between split partials
 };
 
 struct TileInfo {
@@ -163,6 +181,24 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a,
     ti.kb_begin = ti.split * a.kb_per_split;
     ti.kb_end = min(a.k_blocks, ti.kb_begin + a.kb_per_split);
     ti.swap_n = 0;
+    return ti;
+  }
+  if (MODE == kRDX || MODE == kRDW) {
+    // kRDX: m = token block, K = the 2E columns of dL2.
+    // kRDW: m = expert block, then column block, then K split.
+    const int m_tiles = (a.M + kBM - 1) / kBM;
+    const int m = t % m_tiles;
+    const int rest = t / m_tiles;
+    const int n = rest % a.n_tiles;
+    ti.split = MODE == kRDW ? rest / a.n_tiles : 0;
+    ti.swap_n = 0;
+    ti.a_row = m * kBM;
+    ti.rows = min(kBM, a.M - ti.a_row);
+    ti.b_row = m * kBM;
+    ti.b_row2 = 0;
+    ti.out_col = n * 256;
+    ti.kb_begin = ti.split * a.kb_per_split;
+    ti.kb_end = min(a.k_blocks, ti.kb_begin + a.kb_per_split);
     return ti;
   }
   if (ModeInfo<MODE>::wgrad) {
@@ -263,7 +299,7 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
     }
     return;
   }
-  if (ModeInfo<MODE>::wgrad) {
+  if (ModeInfo<MODE>::staged) {
     // fp32 weight-gradient rows; an expert with no token rows gets zeros.
     // Each 32 x 32 chunk goes through this warp's staging tile so that a
     // store instruction writes four whole 128-byte row segments instead of
@@ -271,6 +307,7 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
     const int lane = r & 31;
     const int row0 = ti.a_row + (r & ~31);       // the warp's first row
     const bool empty = ti.kb_end <= ti.kb_begin;
+    float* obase = reinterpret_cast<float*>(a.out) + ti.split * a.split_stride;
 #pragma unroll 1
     for (int c = 32 * half; c < 256; c += 64) {
       float v[32];
@@ -290,12 +327,13 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
         const int col = (lane & 7) * 4;
 #pragma unroll
         for (int rr = 0; rr < 32; rr += 4) {
+          const int row = row0 + rr + sub;
           const float4 q =
               *reinterpret_cast<const float4*>(stage + (rr + sub) * kStageLd + col);
-          *reinterpret_cast<float4*>(
-              reinterpret_cast<float*>(a.out) +
-              static_cast<int64_t>(row0 + rr + sub) * a.out_ld + ti.out_col +
-              c + col) = q;
+          if (a.row_limit == 0 || row < a.row_limit)
+            *reinterpret_cast<float4*>(obase +
+                                       static_cast<int64_t>(row) * a.out_ld +
+                                       ti.out_col + c + col) = q;
         }
         __syncwarp();
       }
@@ -378,6 +416,27 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
         }
       }
     }
+  } else if (MODE == kRDX) {
+    // dx += acc in place (bf16): each element is read and written by this
+    // thread only
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) +
+                         grow * a.out_ld + ti.out_col;
+#pragma unroll 1
+    for (int c = 32 * half; c < 256; c += 64) {
+      float v[32];
+      tmem_ld32(tmem_row + c, v);
+      if (valid && ti.out_col + c < a.out_cols) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+          float o[8];
+          Vec16<__nv_bfloat16>::to_f32(
+              *reinterpret_cast<const uint4*>(out + c + i), o);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) o[q] += v[i + q];
+          st_v4(out + c + i, Vec16<__nv_bfloat16>::from_f32(o));
+        }
+      }
+    }
   } else {
     // kDown, kDH, kDX: 256 bf16 columns
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) +
@@ -455,7 +514,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!aligned) set_status(a.status, MOE_ERR_INVALID);
       }
     }
-  } else if (MODE != kRoute) {
+  } else if (ModeInfo<MODE>::grouped_m) {
     if (warp == 2) {
       int run = 0;
       for (int base = 0; base < a.groups; base += 32) {
@@ -480,7 +539,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (threadIdx.x == 64) {
-    sh.total_tiles = ((a.M + kBM - 1) / kBM) * a.splits;
+    const int m_tiles = (a.M + kBM - 1) / kBM;
+    sh.total_tiles = MODE == kRDX   ? m_tiles * a.n_tiles
+                     : MODE == kRDW ? m_tiles * a.n_tiles * a.splits
+                                    : m_tiles * a.splits;
   }
   if (warp == 1) {
     tmem_alloc(&sh.tmem_base, a.tmem_cols);
@@ -513,10 +575,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint8_t* sa = a_tiles + stage * kATileBytes;
           uint8_t* sb = b_tiles + static_cast<size_t>(stage) * b_tile_bytes;
           if (ModeInfo<MODE>::a_mn) {
-            // two 64-wide MN boxes of 64 K (token) rows
-            tma_load_2d(sa, &tmA, &sh.full[stage], ti.b_row, kb * kBK);
-            tma_load_2d(sa + 8192, &tmA, &sh.full[stage], ti.b_row + 64,
-                        kb * kBK);
+            // two 64-wide MN boxes of 64 K (token) rows; kRDW takes the hi
+            // or lo half of dL2 for even or odd K blocks
+            const int acol = MODE == kRDW ? ti.b_row + (kb & 1) * a.E : ti.b_row;
+            const int arow = MODE == kRDW ? (kb >> 1) * kBK : kb * kBK;
+            tma_load_2d(sa, &tmA, &sh.full[stage], acol, arow);
+            tma_load_2d(sa + 8192, &tmA, &sh.full[stage], acol + 64, arow);
           } else {
             tma_load_2d(sa, &tmA, &sh.full[stage], kb * kBK, ti.a_row);
           }
@@ -527,7 +591,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else if (ModeInfo<MODE>::b_mn) {
             // four 64-wide MN boxes; K rows start at the expert's first K
             // row in B (dgrad) or at the token row itself (wgrad)
-            const int krow = (ModeInfo<MODE>::wgrad ? 0 : ti.b_row) + kb * kBK;
+            const int krow =
+                MODE == kRDX   ? (kb * kBK) % a.E
+                : MODE == kRDW ? (kb >> 1) * kBK
+                               : (ModeInfo<MODE>::wgrad ? 0 : ti.b_row) + kb * kBK;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               tma_load_2d(sb + i * 8192, &tmB, &sh.full[stage],
@@ -675,6 +742,25 @@ inline size_t umma_gemm_smem_bytes(int BN, int stages, bool staging = false) {
   return 1024 + static_cast<size_t>(stages) * (kATileBytes + BN * kBK * 2) +
          ((sizeof(GemmShared) + 15) & ~size_t(15)) +
          (staging ? kStageBytes : 0);
+}
+
+// One persistent launch (one CTA per SM) of a grouped or backward mode.
+template <int MODE>
+inline moe_status launch_umma(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const GemmArgs& g, cudaStream_t stream,
+                              int num_sms) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(umma_gemm_kernel<MODE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             227 * 1024) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  const size_t smem =
+      umma_gemm_smem_bytes(g.BN, g.stages, ModeInfo<MODE>::staged);
+  umma_gemm_kernel<MODE><<<num_sms, kGemmThreads, smem, stream>>>(tmA, tmB, g);
+  return launch_status();
 }
 
 }  // namespace moe

@@ -466,7 +466,13 @@ MOE_API moe_status moe_grouped_ffn_backward(
  *   logits [T, E] fp32 (moe_route's logits_out); topk_idx [T, k];
  *   dlogits [T, E] fp32 out; dw_r [E, D] fp32 out;
  *   workspace >= moe_route_backward_workspace_size(cfg) bytes, 16-byte
- *   aligned (may be NULL when dw_r is NULL).
+ *   aligned (may be NULL when dw_r is NULL, and for bf16 with E and D
+ *   multiples of 64 only when dx is NULL too).
+ * For bf16 with E and D multiples of 64, dw_r and dx run on the tensor
+ * cores: dlogits enters as two bf16 terms hi + lo (hi = bf16(dl),
+ * lo = bf16(dl - hi), about 2^-17 relative) and every product accumulates
+ * in fp32; x, w_r and dx must then be 16-byte aligned.  Otherwise they run
+ * as fp32 sums on the CUDA cores.
  * dw_r and dx are deterministic: fixed-order fp32 sums. */
 MOE_API moe_status moe_route_backward(const moe_route_cfg* cfg, const void* x,
                                       const void* w_r, const float* logits,

@@ -133,6 +133,28 @@ def test_grouped_ffn_reject(lib):
         64 * 256 * 2
 
 
+def test_route_backward_reject(lib):
+    # bf16 with E and D multiples of 64: dx and dw_r run on the tensor cores
+    # through the dL2 workspace, so dx alone needs a workspace
+    tc = L.route_cfg(128, 128, 64, 2, L.MOE_BF16, L.MOE_SCORE_SOFTMAX_TOPK)
+    need = L.moe_route_backward_workspace_size(tc)
+    assert need >= 128 * 2 * 64 * 2            # dL2 [T, 2E] bf16
+    def call(cfg, dw_r, dx, ws, ws_bytes, x=FAKE):
+        return lib.moe_route_backward(ctypes.byref(cfg), x, FAKE, FAKE, FAKE,
+                                      FAKE, FAKE, dw_r, dx, ws, ws_bytes,
+                                      None, None)
+    assert call(tc, None, FAKE, None, 0) == L.MOE_ERR_INVALID
+    assert call(tc, None, FAKE, FAKE, need - 1) == L.MOE_ERR_INVALID
+    assert call(tc, None, FAKE + 8, FAKE, need) == L.MOE_ERR_INVALID
+    assert call(tc, FAKE, None, FAKE, need, x=FAKE + 8) == L.MOE_ERR_INVALID
+    assert call(tc, FAKE, None, FAKE + 8, need) == L.MOE_ERR_INVALID
+    # missing inputs
+    assert call(tc, FAKE, None, FAKE, need, x=None) == L.MOE_ERR_INVALID
+    bad = L.route_cfg(128, 128, 64, 65, L.MOE_BF16, 0)
+    assert L.moe_route_backward_workspace_size(bad) == 0
+    assert call(bad, None, None, None, 0) == L.MOE_ERR_INVALID
+
+
 def test_selftests_reject_null(lib):
     assert lib.moe_selftest_bounded_wait(None, 10, None) == L.MOE_ERR_INVALID
     assert lib.moe_selftest_sigmoid_key(None, None, 5, None) == \

@@ -222,7 +222,12 @@ def test_grouped_ffn_backward_rejects_unaligned_offsets():
     (300, 256, 8, 2, "softmax_topk", (1, 1, 0)),
     (513, 128, 64, 1, "softmax_full", (1, 1, 0)),
     (257, 512, 256, 8, "sigmoid_bias", (8, 4, 2)),
-    (64, 64, 16, 4, "sigmoid_bias", (1, 1, 0))])
+    (64, 64, 16, 4, "sigmoid_bias", (1, 1, 0)),
+    # tensor-core path: D not a multiple of 256, E = 3 x 64, split-K dW_r
+    (200, 384, 128, 8, "softmax_topk", (1, 1, 0)),
+    (130, 1024, 192, 6, "softmax_topk", (1, 1, 0)),
+    (1000, 512, 64, 2, "sigmoid_bias", (4, 2, 2)),
+    (1, 64, 64, 1, "softmax_topk", (1, 1, 0))])
 def test_route_backward_parity(T, D, E, k, score, groups):
     g = torch.Generator().manual_seed(T + E)
     x = torch.randn((T, D), generator=g).to(BF)
