@@ -8,7 +8,11 @@ grouped SwiGLU FFN -> combine) over one batch of seeded synthetic input with
 every input resident in HBM.  The default workload is the Mixtral-like
 top-2 layer (T=2048, D=4096, E=8, k=2, F=14336, bf16, dropless).  Between
 timed steps a 256 MiB buffer (> the 126 MB L2) is overwritten, outside the
-timed events, so every step starts with a cold L2.
+timed events, so every step starts with a cold L2.  After an eager warm-up,
+each of the five calls is captured as its own CUDA graph and the timed loop
+replays them back to back with events between them: the stage times are
+device time, not Python launch overhead.  The end-to-end figure ("e2e") is
+taken through the eager public API with host copies.
 
 Rank 0 prints one JSON line.  Under torchrun (N > 1) every rank runs an
 independent replica on its own GPU with its own seed (weak scaling, no
@@ -34,6 +38,36 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tokens/s at 1 B300; permute+combine GB/s as % of HBM peak"
 FLUSH_BYTES = 256 << 20
+# A bounded GPU spin (about 0.5 ms) before each isolated call of the extras:
+# while it runs the host enqueues the call, so its events measure device time
+# and not the Python launch path.  It sits outside the timed events.
+HOST_AHEAD_CYCLES = 1_000_000
+
+
+def host_ahead():
+    import torch
+    torch.cuda._sleep(HOST_AHEAD_CYCLES)
+
+
+def capture_stages(stages, dev):
+    """Captures each stage function (called with a stream) as its own CUDA
+    graph and returns the graphs.  The stages allocate nothing and never
+    synchronise, and the warm-up before this has set every kernel's
+    shared-memory limit."""
+    import torch
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    for fn in stages:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn(s)
+        graphs.append(g)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return graphs
+
+
 K_graph_cap = 200
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from ncu, keyed by
@@ -209,26 +243,36 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     names = ["route", "layout", "permute", "ffn", "combine"]
 
-    def step(m=None):
-        rec = (lambda j: m[j].record(stream)) if m else (lambda j: None)
-        rec(0)
-        layer.route(x, stream)
-        rec(1)
-        layer.dispatch_layout(idx_in, stream)
-        rec(2)
-        layer.permute(x, stream)
-        rec(3)
-        layer.grouped_ffn(stream)
-        rec(4)
-        layer.combine(gate_in, None, stream)
-        rec(5)
-
+    stages = [lambda s: layer.route(x, s),
+              lambda s: layer.dispatch_layout(idx_in, s),
+              lambda s: layer.permute(x, s),
+              lambda s: layer.grouped_ffn(s),
+              lambda s: layer.combine(gate_in, None, s)]
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        for fn in stages:
+            fn(stream)
     torch.cuda.synchronize()
     if layer.device_status() != 0:
         raise RuntimeError(f"device status {layer.device_status()}")
+    # each stage as its own CUDA graph: a replay is one cheap host call, so
+    # the host stays ahead of the GPU and the events between replays measure
+    # device time, with the GPU busy throughout (no Python launch gaps, no
+    # idle time that would lift it off its power cap)
+    graphs = capture_stages(stages, dev)
+
+    def step(m=None):
+        for j, g in enumerate(graphs):
+            if m:
+                m[j].record(stream)
+            g.replay()
+        if m:
+            m[5].record(stream)
+
+    for _ in range(3):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     marks = [[ev() for _ in range(6)] for _ in range(args.steps)]
@@ -369,7 +413,9 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
                    "active_experts": active,
                    "routing": wl.routing or "router",
                    "parallelism": f"replicas x{world}",
-                   "l2": "flushed (256 MiB write) before every timed step"},
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "launch": "each stage replayed as its own CUDA graph, "
+                             "back to back: stage times are device time"},
         "kernels": kernels,
         "permute_combine": {"gbs": round(pc_gbs, 1),
                             "frac_of_hbm": round(pc_gbs / peaks["hbm_gbs"], 4),
@@ -441,6 +487,7 @@ def run_extras(args, local_rank, workload):
             fn()
         ts = []
         for _ in range(reps):
+            host_ahead()
             flush.zero_()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)

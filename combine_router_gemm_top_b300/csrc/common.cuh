@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -28,6 +30,23 @@ inline bool aligned(const void* p, uintptr_t a) {
 inline moe_status launch_status() {
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (the
+// attribute belongs to each device's context); `done` has one bit per
+// device ordinal.
+inline bool set_smem_limit_once(const void* func, int bytes,
+                                std::atomic<uint64_t>* done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return false;
+  const uint64_t bit = 1ull << dev;
+  if (done->load(std::memory_order_acquire) & bit) return true;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           bytes) != cudaSuccess)
+    return false;
+  done->fetch_or(bit, std::memory_order_release);
+  return true;
 }
 
 inline size_t dtype_bytes(int32_t dtype) {

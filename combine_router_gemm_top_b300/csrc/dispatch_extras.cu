@@ -18,16 +18,18 @@
 namespace moe {
 
 constexpr int kMatrixThreads = 256;
-constexpr int kMatrixPairsPerBlock = 8192;
+constexpr int kMatrixPairsPerBlock = 1024;
 
 __global__ void zero_i32_kernel(int32_t* p, int64_t n) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i < n) p[i] = 0;
 }
 
-// grid (chunks, n_src): block (c, s) counts pairs [c*8192, (c+1)*8192) of
+// grid (chunks, n_src): block (c, s) counts pairs [c*1024, (c+1)*1024) of
 // source shard s into a shared histogram over destinations, then adds it
-// to row s of the matrix.
+// to row s of the matrix.  Each warp takes 32 consecutive pairs at a time;
+// lanes with the same destination are counted together (one shared atomic
+// per distinct destination in the warp).
 __global__ void __launch_bounds__(kMatrixThreads)
     dispatch_matrix_kernel(int64_t pairs_per_src, int k, int E, int n_dst,
                            const int32_t* __restrict__ topk_idx,
@@ -40,15 +42,25 @@ __global__ void __launch_bounds__(kMatrixThreads)
   const int64_t lo = static_cast<int64_t>(blockIdx.x) * kMatrixPairsPerBlock;
   const int64_t hi = min(pairs_per_src, lo + kMatrixPairsPerBlock);
   const int epr = E / n_dst;
-  for (int64_t q = lo + threadIdx.x; q < hi; q += blockDim.x) {
-    const int64_t p = base + q;
-    if (dst_row != nullptr && __ldg(dst_row + p) < 0) continue;
-    const int e = __ldg(topk_idx + p);
-    if (e < 0 || e >= E) {
-      set_status(status, MOE_ERR_INDEX);
-      continue;
+  const int lane = threadIdx.x & 31;
+  // q0 is the same on every lane of a warp, so each warp runs whole
+  // iterations (the match below needs all 32 lanes)
+  for (int64_t q0 = lo + (threadIdx.x & ~31); q0 < hi; q0 += blockDim.x) {
+    const int64_t q = q0 + lane;
+    int d = -1;
+    if (q < hi) {
+      const int64_t p = base + q;
+      const int32_t row = dst_row != nullptr ? __ldg(dst_row + p) : 0;
+      const int e = __ldg(topk_idx + p);
+      if (row >= 0) {
+        if (e < 0 || e >= E)
+          set_status(status, MOE_ERR_INDEX);
+        else
+          d = e / epr;
+      }
     }
-    atomicAdd(&hist[e / epr], 1);
+    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    if (d >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
   }
   __syncthreads();
   int32_t* row = matrix + static_cast<int64_t>(blockIdx.y) * n_dst;

@@ -187,15 +187,10 @@ moe_status launch_layout(int T, int k, int E, int R, int capacity,
       n_dropped, rank_send_counts, rank_send_displs);
   if (nchunks > 0) {
     const size_t smem = (kLayoutWarps + 1) * E * sizeof(int32_t);
-    static bool attr_set = false;
-    if (!attr_set) {
-      if (cudaFuncSetAttribute(layout_assign_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (kLayoutWarps + 1) * kLayoutMaxE * 4) !=
-          cudaSuccess)
-        return MOE_ERR_CUDA;
-      attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (!set_smem_limit_once(reinterpret_cast<const void*>(layout_assign_kernel),
+                             (kLayoutWarps + 1) * kLayoutMaxE * 4, &attr_done))
+      return MOE_ERR_CUDA;
     layout_assign_kernel<<<nchunks, 256, smem, stream>>>(
         P, E, capacity, topk_idx, w, expert_offsets, dst_row, src_pair);
   }

@@ -354,14 +354,11 @@ moe_status launch_route(const moe_route_cfg& c, const void* x, const void* w_r,
     g.status = status;
     g.wait_limit_ns = kWaitLimitNs;
     const size_t smem = umma_gemm_smem_bytes(g.BN, g.stages);
-    static bool attr_set = false;
-    if (!attr_set) {
-      if (cudaFuncSetAttribute(umma_gemm_kernel<kRoute>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               227 * 1024) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      attr_set = true;
-    }
+    static std::atomic<uint64_t> attr_done{0};
+    if (!set_smem_limit_once(
+            reinterpret_cast<const void*>(umma_gemm_kernel<kRoute>),
+            227 * 1024, &attr_done))
+      return MOE_ERR_CUDA;
     const int tiles = static_cast<int>(ceil_div(c.T, kBM)) * p.splits;
     const int grid = tiles < num_sms ? tiles : num_sms;
     umma_gemm_kernel<kRoute><<<grid, kGemmThreads, smem, stream>>>(tmA, tmB, g);

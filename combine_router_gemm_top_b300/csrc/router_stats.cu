@@ -6,9 +6,14 @@
 // Dispatch: bias terms on the routing scores adjusted to keep the load
 // balanced).
 //
-// Two deterministic launches: per-block partial sums (fp64 probability
-// sums, int32 routed counts) over a fixed token order, then one block of 32
-// warps that adds the partials in a fixed order and forms f, P and L_aux.
+// One memset and one kernel.  Each warp takes tokens, evaluates the router
+// probabilities in fp32 and rounds each to a multiple of 2^-32; warps add
+// their sums into the block's shared uint64 accumulators, and blocks add
+// theirs into global ones.  The sums are exact 64-bit integers (below 2^63
+// for T < 2^31; the error on P_e is below 2^-33), so they do not depend on
+// the order of the additions and the results are deterministic.  Routed
+// counts are added the same way.  The last block to finish forms f, P and
+// L_aux, adding f_i * P_i through a fixed tree.
 #include <float.h>
 
 #include "common.cuh"
@@ -17,6 +22,8 @@
 namespace moe {
 
 constexpr int kStatsWarps = 8;
+constexpr float kFix = 4294967296.0f;          // 2^32
+constexpr double kInvFix = 1.0 / 4294967296.0;
 
 __device__ __forceinline__ float stats_warp_sum(float v) {
 #pragma unroll
@@ -30,25 +37,37 @@ __device__ __forceinline__ float stats_warp_max(float v) {
   return v;
 }
 
+struct StatsAcc {
+  unsigned long long p[256];   // sum of p_e in units of 2^-32
+  unsigned int cnt[256];       // routed pairs of expert e
+  unsigned int done;           // blocks finished
+};
+
 // One warp per token (grid-stride); lane l holds experts l + 32 i.
 template <int NI>
 __global__ void __launch_bounds__(kStatsWarps * 32)
-    router_stats_partial_kernel(int T, int E, int k, int score,
-                                const float* __restrict__ logits,
-                                const int32_t* __restrict__ topk_idx,
-                                double* __restrict__ part_p,
-                                int32_t* __restrict__ part_cnt,
-                                int32_t* status) {
-  __shared__ double s_p[kStatsWarps][NI * 32];
-  __shared__ int32_t s_cnt[NI * 32];
+    router_stats_kernel(int T, int E, int k, int score, float alpha,
+                        const float* __restrict__ logits,
+                        const int32_t* __restrict__ topk_idx,
+                        StatsAcc* __restrict__ acc_g, float* __restrict__ f,
+                        float* __restrict__ P,
+                        int32_t* __restrict__ counts_routed,
+                        float* __restrict__ aux_loss, int32_t* status) {
+  __shared__ unsigned long long s_p[NI * 32];
+  __shared__ unsigned int s_cnt[NI * 32];
+  __shared__ unsigned int s_ticket;
+  __shared__ double s_fp[kStatsWarps];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < NI * 32; i += blockDim.x) s_cnt[i] = 0;
+  for (int i = threadIdx.x; i < NI * 32; i += blockDim.x) {
+    s_p[i] = 0ull;
+    s_cnt[i] = 0u;
+  }
   __syncthreads();
 
-  double acc[NI];
+  unsigned long long acc[NI];
 #pragma unroll
-  for (int i = 0; i < NI; ++i) acc[i] = 0.0;
+  for (int i = 0; i < NI; ++i) acc[i] = 0ull;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kStatsWarps;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kStatsWarps + warp;
        t < T; t += stride) {
@@ -86,81 +105,60 @@ __global__ void __launch_bounds__(kStatsWarps * 32)
       for (int i = 0; i < NI; ++i) p[i] = p[i] / z;
     }
 #pragma unroll
-    for (int i = 0; i < NI; ++i) acc[i] += static_cast<double>(p[i]);
+    for (int i = 0; i < NI; ++i) acc[i] += __float2ull_rn(p[i] * kFix);
     if (lane < k) {
       const int e = topk_idx[t * k + lane];
       if (e >= 0 && e < E)
-        atomicAdd(&s_cnt[e], 1);
+        atomicAdd(&s_cnt[e], 1u);
       else
         set_status(status, MOE_ERR_INDEX);
     }
   }
 #pragma unroll
-  for (int i = 0; i < NI; ++i) s_p[warp][lane + 32 * i] = acc[i];
+  for (int i = 0; i < NI; ++i)
+    if (lane + 32 * i < E && acc[i] != 0ull) atomicAdd(&s_p[lane + 32 * i], acc[i]);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    double s = 0.0;
-    for (int w = 0; w < kStatsWarps; ++w) s += s_p[w][e];
-    part_p[static_cast<int64_t>(blockIdx.x) * E + e] = s;
-    part_cnt[static_cast<int64_t>(blockIdx.x) * E + e] = s_cnt[e];
+    if (s_p[e] != 0ull) atomicAdd(&acc_g->p[e], s_p[e]);
+    if (s_cnt[e] != 0u) atomicAdd(&acc_g->cnt[e], s_cnt[e]);
   }
-}
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = atomicAdd(&acc_g->done, 1u);
+  __syncthreads();
+  if (s_ticket != gridDim.x - 1) return;
 
-// One block of 32 warps: warp w sums the partials of experts w, w+32, ...
-// (lane-strided over blocks, then a fixed xor tree), and the block adds
-// f_i * P_i over experts in a fixed order.  Deterministic.
-constexpr int kFinalWarps = 32;
-
-__global__ void __launch_bounds__(kFinalWarps * 32)
-    router_stats_final_kernel(int T, int E, int k, int blocks, float alpha,
-                              const double* __restrict__ part_p,
-                              const int32_t* __restrict__ part_cnt,
-                              float* __restrict__ f, float* __restrict__ P,
-                              int32_t* __restrict__ counts_routed,
-                              float* __restrict__ aux_loss) {
-  __shared__ double s_fp[kFinalWarps];
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  // the last block: every block's additions are visible
+  __threadfence();
   const double pairs = static_cast<double>(T) * k;
-  double local = 0.0;
-  for (int e = warp; e < E; e += kFinalWarps) {
-    double sp = 0.0;
-    long long c = 0;
-    for (int b = lane; b < blocks; b += 32) {
-      sp += part_p[static_cast<int64_t>(b) * E + e];
-      c += part_cnt[static_cast<int64_t>(b) * E + e];
-    }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      sp += __shfl_xor_sync(0xffffffffu, sp, d);
-      c += __shfl_xor_sync(0xffffffffu, c, d);
-    }
-    const double fe = pairs > 0 ? static_cast<double>(c) / pairs : 0.0;
-    const double pe = T > 0 ? sp / static_cast<double>(T) : 0.0;
-    if (lane == 0) {
-      f[e] = static_cast<float>(fe);
-      P[e] = static_cast<float>(pe);
-      if (counts_routed != nullptr) counts_routed[e] = static_cast<int32_t>(c);
-    }
-    local += fe * pe;
+  double fp = 0.0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const unsigned long long sum = atomicAdd(&acc_g->p[e], 0ull);
+    const unsigned int cnt = atomicAdd(&acc_g->cnt[e], 0u);
+    const double fe = pairs > 0 ? static_cast<double>(cnt) / pairs : 0.0;
+    const double pe =
+        T > 0 ? static_cast<double>(sum) * kInvFix / static_cast<double>(T)
+              : 0.0;
+    f[e] = static_cast<float>(fe);
+    P[e] = static_cast<float>(pe);
+    if (counts_routed != nullptr) counts_routed[e] = static_cast<int32_t>(cnt);
+    fp += fe * pe;
   }
-  if (lane == 0) s_fp[warp] = local;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) fp += __shfl_xor_sync(0xffffffffu, fp, d);
+  if (lane == 0) s_fp[warp] = fp;
   __syncthreads();
   if (threadIdx.x == 0) {
-    double s = 0.0;
-    for (int w = 0; w < kFinalWarps; ++w) s += s_fp[w];
-    aux_loss[0] = static_cast<float>(static_cast<double>(alpha) * E * s);
+    double sum = 0.0;
+    for (int w = 0; w < kStatsWarps; ++w) sum += s_fp[w];
+    aux_loss[0] = static_cast<float>(static_cast<double>(alpha) * E * sum);
   }
-}
-
-int router_stats_blocks(int T) {
-  const int64_t want = ceil_div(T, kStatsWarps);
-  return static_cast<int>(want < kNumSMs ? (want > 0 ? want : 1) : kNumSMs);
 }
 
 size_t router_stats_ws_bytes(int T, int E) {
-  const size_t b = static_cast<size_t>(router_stats_blocks(T));
-  return b * E * (sizeof(double) + sizeof(int32_t)) + 256;
+  (void)T;
+  (void)E;
+  return sizeof(StatsAcc);
 }
 
 moe_status launch_router_stats(int T, int E, int k, int score,
@@ -169,26 +167,32 @@ moe_status launch_router_stats(int T, int E, int k, int score,
                                int32_t* counts_routed, float* aux_loss,
                                void* ws, int32_t* status,
                                cudaStream_t stream) {
-  const int blocks = router_stats_blocks(T);
-  double* part_p = static_cast<double*>(ws);
-  int32_t* part_cnt = reinterpret_cast<int32_t*>(
-      static_cast<uint8_t*>(ws) + static_cast<size_t>(blocks) * E * sizeof(double));
+  StatsAcc* acc = static_cast<StatsAcc*>(ws);
+  if (cudaMemsetAsync(acc, 0, sizeof(StatsAcc), stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  // one token per warp up to 4 blocks per SM, then a grid-stride loop
+  const int64_t want = ceil_div(T, kStatsWarps);
+  const int64_t cap = 4 * kNumSMs;
+  const unsigned blocks =
+      static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
   const int ni = static_cast<int>(ceil_div(E, 32));
-  const dim3 grid(static_cast<unsigned>(blocks)), block(kStatsWarps * 32);
+  const dim3 block(kStatsWarps * 32);
   if (ni <= 1)
-    router_stats_partial_kernel<1><<<grid, block, 0, stream>>>(
-        T, E, k, score, logits, topk_idx, part_p, part_cnt, status);
+    router_stats_kernel<1><<<blocks, block, 0, stream>>>(
+        T, E, k, score, alpha, logits, topk_idx, acc, f, P, counts_routed,
+        aux_loss, status);
   else if (ni <= 2)
-    router_stats_partial_kernel<2><<<grid, block, 0, stream>>>(
-        T, E, k, score, logits, topk_idx, part_p, part_cnt, status);
+    router_stats_kernel<2><<<blocks, block, 0, stream>>>(
+        T, E, k, score, alpha, logits, topk_idx, acc, f, P, counts_routed,
+        aux_loss, status);
   else if (ni <= 4)
-    router_stats_partial_kernel<4><<<grid, block, 0, stream>>>(
-        T, E, k, score, logits, topk_idx, part_p, part_cnt, status);
+    router_stats_kernel<4><<<blocks, block, 0, stream>>>(
+        T, E, k, score, alpha, logits, topk_idx, acc, f, P, counts_routed,
+        aux_loss, status);
   else
-    router_stats_partial_kernel<8><<<grid, block, 0, stream>>>(
-        T, E, k, score, logits, topk_idx, part_p, part_cnt, status);
-  router_stats_final_kernel<<<1, kFinalWarps * 32, 0, stream>>>(
-      T, E, k, blocks, alpha, part_p, part_cnt, f, P, counts_routed, aux_loss);
+    router_stats_kernel<8><<<blocks, block, 0, stream>>>(
+        T, E, k, score, alpha, logits, topk_idx, acc, f, P, counts_routed,
+        aux_loss, status);
   return launch_status();
 }
 

@@ -749,14 +749,10 @@ template <int MODE>
 inline moe_status launch_umma(const CUtensorMap& tmA, const CUtensorMap& tmB,
                               const GemmArgs& g, cudaStream_t stream,
                               int num_sms) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(umma_gemm_kernel<MODE>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             227 * 1024) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  if (!set_smem_limit_once(reinterpret_cast<const void*>(umma_gemm_kernel<MODE>),
+                           227 * 1024, &attr_done))
+    return MOE_ERR_CUDA;
   const size_t smem =
       umma_gemm_smem_bytes(g.BN, g.stages, ModeInfo<MODE>::staged);
   umma_gemm_kernel<MODE><<<num_sms, kGemmThreads, smem, stream>>>(tmA, tmB, g);

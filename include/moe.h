@@ -277,9 +277,11 @@ MOE_API size_t moe_router_stats_workspace_size(int32_t T, int32_t E);
  *   aux_loss       [1] fp32 out: alpha * E * sum_i f_i P_i
  *   workspace      >= moe_router_stats_workspace_size(T, E) bytes, 16-byte
  *                  aligned
- * Probabilities are evaluated in fp32 and summed in fp64 in a fixed order:
- * the results are deterministic.  Ids outside [0, E) are skipped and raise
- * MOE_ERR_INDEX in `status`.  E <= 256, 1 <= k <= min(E, 32). */
+ * Probabilities are evaluated in fp32, rounded to multiples of 2^-32 and
+ * summed exactly as 64-bit integers (T < 2^31): the results do not depend on
+ * the order of the additions and are deterministic.  Ids outside [0, E) are
+ * skipped and raise MOE_ERR_INDEX in `status`.  E <= 256,
+ * 1 <= k <= min(E, 32). */
 MOE_API moe_status moe_router_stats(int32_t T, int32_t E, int32_t k,
                                     int32_t score, const float* logits,
                                     const int32_t* topk_idx, float alpha,

@@ -358,6 +358,10 @@ FFN_CASES = [
      torch.bfloat16),
     (7, 320, 128, [40, 170, 3, 81, 128 + 65, 0, 97], torch.bfloat16),
     (2, 768, 384, [1, 64], torch.bfloat16),
+    # long down-projection contractions (32 and 16 K blocks) over few tiles,
+    # swapped and normal
+    (4, 512, 2048, [300, 40, 0, 129], torch.bfloat16),
+    (1, 256, 1024, [1000], torch.bfloat16),
 ]
 
 
