@@ -9,9 +9,11 @@
 // Pairs are cut into chunks of 2048 (one block each), each chunk into 8
 // warp sub-chunks of 256.  Three launches:
 //   1 layout_hist    per-chunk expert histograms  -> ws[chunk][E]
-//   2 layout_scan    (one block) per expert: exclusive prefix over chunks
-//                    (in place), totals, capacity clamp, offsets, rank
-//                    counts and displacements, n_kept, n_dropped
+//   2 layout_scan    (one block) per expert, its chunk column cut into
+//                    segments over the block's threads: exclusive prefix
+//                    over chunks (in place), totals, capacity clamp,
+//                    offsets, rank counts and displacements, n_kept,
+//                    n_dropped
 //   3 layout_assign  per chunk: per-warp sub-chunk prefixes, then each warp
 //                    walks its pairs in order, ranking equal experts inside
 //                    a 32-pair step with __match_any_sync; pos = earlier
@@ -54,15 +56,43 @@ __global__ void __launch_bounds__(1024)
                        int32_t* n_dropped, int32_t* rank_send_counts,
                        int32_t* rank_send_displs) {
   __shared__ int32_t kept[kLayoutMaxE];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int32_t run = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      int32_t* cell = ws + static_cast<int64_t>(c) * E + e;
-      const int32_t v = *cell;
-      *cell = run;        // exclusive prefix of earlier chunks
-      run += v;
+  __shared__ int32_t seg_sum[1024];
+  {
+    // the chunk column of each expert (E <= 1024) is cut into S = 1024 / E
+    // segments; thread (s, e) = (tid / E, tid % E) first adds its segment
+    // (independent loads), then rewrites it as the exclusive prefix,
+    // starting from the sum of the earlier segments
+    const int S = 1024 / E;
+    const int seg = (nchunks + S - 1) / S;
+    const int e = threadIdx.x % E;
+    const int sg = threadIdx.x / E;
+    const bool on = sg < S;
+    const int c_begin = sg * seg;
+    const int c_end = min(nchunks, c_begin + seg);
+    int32_t mine = 0;
+    if (on) {
+#pragma unroll 4
+      for (int c = c_begin; c < c_end; ++c)
+        mine += ws[static_cast<int64_t>(c) * E + e];
     }
-    kept[e] = capacity > 0 ? min(run, capacity) : run;
+    seg_sum[threadIdx.x] = mine;
+    __syncthreads();
+    if (on) {
+      int32_t run = 0;
+      for (int q = 0; q < sg; ++q) run += seg_sum[q * E + e];
+      for (int c0 = c_begin; c0 < c_end; c0 += 8) {
+        int32_t v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          v[i] = c0 + i < c_end ? ws[static_cast<int64_t>(c0 + i) * E + e] : 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (c0 + i < c_end) ws[static_cast<int64_t>(c0 + i) * E + e] = run;
+          run += v[i];
+        }
+      }
+      if (sg == S - 1) kept[e] = capacity > 0 ? min(run, capacity) : run;
+    }
   }
   __syncthreads();
   // exclusive scan of kept[0..E): each of 32 lanes of warp 0 scans a

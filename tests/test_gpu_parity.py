@@ -116,6 +116,8 @@ LAYOUT_CASES = [
     (5000, 4, 64, 16, 0, "one"), (5000, 4, 64, 16, 100, "one"),
     (3001, 8, 256, 8, 100, "dup"), (4096, 8, 256, 8, 0, "distinct"),
     (1500, 3, 1024, 32, 2, "dup"), (65536, 8, 128, 8, 0, "distinct"),
+    # more than 256 chunks of 2048 pairs: the scan takes several batches
+    (70000, 8, 64, 8, 0, "dup"),
 ]
 
 
@@ -230,6 +232,13 @@ ROUTE_CASES = [
     (400, 256, 256, 8, torch.bfloat16, "sigmoid_bias", (32, 6, 2), None, None, 0.1),
     # E not a multiple of 32, groups straddling lanes
     (211, 128, 200, 7, torch.bfloat16, "sigmoid_bias", (8, 3, 5), None, None, 0.1),
+    # many row blocks, one K split, ragged last row block
+    (10000, 256, 128, 8, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
+    (9500, 128, 64, 1, torch.bfloat16, "softmax_full", (1, 1, 0), None, 1.5, None),
+    (12000, 64, 8, 2, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
+    (20000, 128, 200, 5, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
+    (10000, 128, 64, 9, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
+    (10000, 128, 64, 4, torch.bfloat16, "softmax_topk", (4, 2, 2), None, None, None),
 ]
 
 
@@ -242,10 +251,11 @@ def test_route_parity(case):
     check_route(x, w, off, b, k, score, groups, idx, gate, logits)
 
 
-def test_route_ties_go_to_lower_index():
+@pytest.mark.parametrize("T", [512, 10240])
+def test_route_ties_go_to_lower_index(T):
     # D = E and w_r = identity: logits equal x exactly (small integers in
     # bf16), so many experts tie; the lower index must win every tie
-    T, E, k = 512, 16, 4
+    E, k = 16, 4
     rng = np.random.default_rng(3)
     xl = rng.integers(-2, 3, size=(T, E)).astype(np.float32)
     x = torch.tensor(xl).to(torch.bfloat16)
