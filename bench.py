@@ -169,7 +169,9 @@ def build_layer(wl, device, seed):
 
 
 def launches_per_step(layer, routed):
-    n = 3 + 1 + 1                # layout (3), permute, combine
+    from combine_router_gemm_top_b300 import _lib as L
+    # layout (one block, or histogram + scan + assignment), permute, combine
+    n = L.moe_dispatch_layout_launches(layer.T, layer.k, layer.E) + 1 + 1
     if routed:
         n += 2                   # route: router GEMM + select
     if not layer.identity:

@@ -34,7 +34,8 @@ SCORE_CODES = {"softmax_topk": MOE_SCORE_SOFTMAX_TOPK,
                "sigmoid_bias": MOE_SCORE_SIGMOID_BIAS}
 
 EXPORTED = ["moe_route_workspace_size", "moe_route",
-            "moe_dispatch_layout_workspace_size", "moe_dispatch_layout",
+            "moe_dispatch_layout_workspace_size",
+            "moe_dispatch_layout_launches", "moe_dispatch_layout",
             "moe_permute", "moe_grouped_ffn_workspace_size",
             "moe_grouped_ffn", "moe_combine", "moe_selftest_bounded_wait",
             "moe_selftest_sigmoid_key", "moe_dispatch_layout_noalloc",
@@ -73,6 +74,7 @@ _SIGS = {
     "moe_route": (_i32, [ctypes.POINTER(RouteCfg), _vp, _vp, _vp, _vp, _vp,
                          _vp, _vp, _vp, _sz, _vp, _vp]),
     "moe_dispatch_layout_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "moe_dispatch_layout_launches": (_i32, [_i32, _i32, _i32]),
     "moe_dispatch_layout": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _vp,
                                    _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                    _sz, _vp, _vp]),
@@ -196,6 +198,10 @@ def moe_route(cfg, x, w_r, logit_offset, sel_bias, topk_idx, topk_gate,
 
 def moe_dispatch_layout_workspace_size(T, k, E) -> int:
     return load().moe_dispatch_layout_workspace_size(T, k, E)
+
+
+def moe_dispatch_layout_launches(T, k, E) -> int:
+    return load().moe_dispatch_layout_launches(T, k, E)
 
 
 def moe_dispatch_layout(T, k, E, R, capacity, topk_idx, expert_counts,

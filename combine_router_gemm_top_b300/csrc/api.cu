@@ -141,6 +141,11 @@ size_t moe_dispatch_layout_workspace_size(int32_t T, int32_t k, int32_t E) {
   return layout_ws_bytes(static_cast<int64_t>(T) * k, E);
 }
 
+int32_t moe_dispatch_layout_launches(int32_t T, int32_t k, int32_t E) {
+  if (T < 0 || k < 1 || k > 32 || E < 1 || E > kLayoutMaxE) return 0;
+  return layout_launches(static_cast<int64_t>(T) * k, E);
+}
+
 moe_status moe_dispatch_layout(int32_t T, int32_t k, int32_t E, int32_t R,
                                int32_t capacity, const int32_t* topk_idx,
                                int32_t* expert_counts, int32_t* expert_offsets,

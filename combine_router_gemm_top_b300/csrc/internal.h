@@ -50,6 +50,7 @@ constexpr int kLayoutChunk = 2048;   // pairs per layout block
 constexpr int kLayoutMaxE = 1024;
 constexpr int kMaxGroupsApi = 1024;   // experts the grouped tcgen05 scheduler handles
 size_t layout_ws_bytes(int64_t P, int E);
+int layout_launches(int64_t P, int E);
 moe_status launch_layout(int T, int k, int E, int R, int capacity,
                          const int32_t* topk_idx, int32_t* expert_counts,
                          int32_t* expert_offsets, int32_t* dst_row,

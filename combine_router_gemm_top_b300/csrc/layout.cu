@@ -6,8 +6,9 @@
 // expert_parallel_dispatch listing: destination = expert /
 // experts_per_device and the bincount of destinations).
 //
-// Pairs are cut into chunks of 2048 (one block each), each chunk into 8
-// warp sub-chunks of 256.  Three launches:
+// Up to 16384 pairs and 256 experts: one block does the whole layout
+// (layout_small).  Beyond that, pairs are cut into chunks of 2048 (one block
+// each), each chunk into 8 warp sub-chunks of 256.  Three launches:
 //   1 layout_hist    per-chunk expert histograms  -> ws[chunk][E]
 //   2 layout_scan    (one block) per expert, its chunk column cut into
 //                    segments over the block's threads: exclusive prefix
@@ -47,6 +48,55 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   int32_t* out = ws + static_cast<int64_t>(blockIdx.x) * E;
   for (int e = threadIdx.x; e < E; e += blockDim.x) out[e] = hist[e];
+}
+
+// From the kept count of every expert (shared memory, one block): the
+// exclusive scan into offsets, the counts, n_kept, n_dropped, and each
+// rank's send count and displacement.  off_s (shared) also receives the
+// offsets when not null.
+__device__ void layout_finish(int64_t P, int E, int R, const int32_t* kept,
+                              int32_t* off_s, int32_t* expert_counts,
+                              int32_t* expert_offsets, int32_t* n_kept,
+                              int32_t* n_dropped, int32_t* rank_send_counts,
+                              int32_t* rank_send_displs) {
+  // exclusive scan of kept[0..E): each of 32 lanes of warp 0 scans a
+  // contiguous segment, then the segment sums are scanned across lanes
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int seg = (E + 31) / 32;
+    const int b = lane * seg;
+    const int en = min(E, b + seg);
+    int32_t s = 0;
+    for (int e = b; e < en; ++e) s += kept[e];
+    int32_t incl = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int32_t run = incl - s;      // exclusive start of this lane's segment
+    for (int e = b; e < en; ++e) {
+      expert_offsets[e] = run;
+      if (off_s != nullptr) off_s[e] = run;
+      expert_counts[e] = kept[e];
+      run += kept[e];
+    }
+    if (lane == 31) {
+      expert_offsets[E] = incl;
+      *n_kept = incl;
+      *n_dropped = static_cast<int32_t>(P - incl);
+    }
+  }
+  __syncthreads();
+  // rank r owns experts [r*E/R, (r+1)*E/R): its rows are one contiguous run
+  const int epr = E / R;
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
+    int32_t start = 0, cnt = 0;
+    for (int e = 0; e < r * epr; ++e) start += kept[e];
+    for (int e = r * epr; e < (r + 1) * epr; ++e) cnt += kept[e];
+    rank_send_counts[r] = cnt;
+    rank_send_displs[r] = start;
+  }
 }
 
 __global__ void __launch_bounds__(1024)
@@ -95,43 +145,8 @@ __global__ void __launch_bounds__(1024)
     }
   }
   __syncthreads();
-  // exclusive scan of kept[0..E): each of 32 lanes of warp 0 scans a
-  // contiguous segment, then the segment sums are scanned across lanes
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const int seg = (E + 31) / 32;
-    const int b = lane * seg;
-    const int en = min(E, b + seg);
-    int32_t s = 0;
-    for (int e = b; e < en; ++e) s += kept[e];
-    int32_t incl = s;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
-    }
-    int32_t run = incl - s;      // exclusive start of this lane's segment
-    for (int e = b; e < en; ++e) {
-      expert_offsets[e] = run;
-      expert_counts[e] = kept[e];
-      run += kept[e];
-    }
-    if (lane == 31) {
-      expert_offsets[E] = incl;
-      *n_kept = incl;
-      *n_dropped = static_cast<int32_t>(P - incl);
-    }
-  }
-  __syncthreads();
-  // rank r owns experts [r*E/R, (r+1)*E/R): its rows are one contiguous run
-  const int epr = E / R;
-  for (int r = threadIdx.x; r < R; r += blockDim.x) {
-    int32_t start = 0, cnt = 0;
-    for (int e = 0; e < r * epr; ++e) start += kept[e];
-    for (int e = r * epr; e < (r + 1) * epr; ++e) cnt += kept[e];
-    rank_send_counts[r] = cnt;
-    rank_send_displs[r] = start;
-  }
+  layout_finish(P, E, R, kept, nullptr, expert_counts, expert_offsets, n_kept,
+                n_dropped, rank_send_counts, rank_send_displs);
 }
 
 __global__ void __launch_bounds__(256)
@@ -194,6 +209,87 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The whole layout in one block of 32 warps, for up to kSmallP pairs and
+// kSmallE experts.  Warp w owns a contiguous range of pairs (whole 32-pair
+// steps); it counts its experts, a prefix over warps gives each warp the
+// pairs of each expert before its range, the scan and capacity clamp follow,
+// then each warp walks its range in order, ranking equal experts inside a
+// 32-pair step with __match_any_sync exactly as layout_assign does.
+constexpr int64_t kSmallP = 16384;
+constexpr int kSmallE = 256;
+constexpr int kSmallWarps = 32;
+
+__global__ void __launch_bounds__(kSmallWarps * 32)
+    layout_small_kernel(int64_t P, int E, int R, int capacity,
+                        const int32_t* __restrict__ idx,
+                        int32_t* expert_counts, int32_t* expert_offsets,
+                        int32_t* dst_row, int32_t* src_pair, int32_t* n_kept,
+                        int32_t* n_dropped, int32_t* rank_send_counts,
+                        int32_t* rank_send_displs, int32_t* status) {
+  extern __shared__ int32_t sm[];
+  int32_t* whist = sm;                          // [32][E]
+  int32_t* kept = sm + kSmallWarps * E;         // [E]
+  int32_t* off = kept + E;                      // [E]
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) whist[i] = 0;
+  __syncthreads();
+  const int64_t span = ceil_div(ceil_div(P, kSmallWarps), 32) * 32;
+  const int64_t s0 = static_cast<int64_t>(warp) * span;
+  const int64_t s1 = min(P, s0 + span);
+  bool bad = false;
+  for (int64_t p = s0 + lane; p < s1; p += 32) {
+    const int e = __ldg(idx + p);
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E))
+      atomicAdd(&whist[warp * E + e], 1);
+    else
+      bad = true;
+  }
+  if (bad) set_status(status, MOE_ERR_INDEX);
+  __syncthreads();
+  // whist[w][e] <- pairs of expert e before warp w's range; kept = clamp
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t run = 0;
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const int32_t v = whist[w * E + e];
+      whist[w * E + e] = run;
+      run += v;
+    }
+    kept[e] = capacity > 0 ? min(run, capacity) : run;
+  }
+  __syncthreads();
+  layout_finish(P, E, R, kept, off, expert_counts, expert_offsets, n_kept,
+                n_dropped, rank_send_counts, rank_send_displs);
+  __syncthreads();
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int32_t* my = whist + warp * E;
+  for (int64_t pb = s0; pb < s1; pb += 32) {
+    const int64_t p = pb + lane;
+    const bool in = p < s1;
+    const int e = in ? __ldg(idx + p) : -1;
+    const bool valid = in && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    // lanes with the same expert id (invalid lanes get distinct keys)
+    const int key = valid ? e : -1 - lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    int32_t pos = 0;
+    if (valid) pos = my[e] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (valid && (peers & lt_mask) == 0) my[e] += __popc(peers);
+    __syncwarp();
+    if (in) {
+      const bool kept_p = valid && (capacity <= 0 || pos < capacity);
+      const int32_t r = kept_p ? off[e] + pos : -1;
+      dst_row[p] = r;
+      if (kept_p) src_pair[r] = static_cast<int32_t>(p);
+    }
+  }
+}
+
+int layout_launches(int64_t P, int E) {
+  if (P <= kSmallP && E <= kSmallE) return 1;
+  return P > 0 ? 3 : 1;
+}
+
 size_t layout_ws_bytes(int64_t P, int E) {
   const int64_t nchunks = ceil_div(P, kLayoutChunk);
   return static_cast<size_t>(nchunks > 0 ? nchunks : 1) * E * sizeof(int32_t);
@@ -207,6 +303,14 @@ moe_status launch_layout(int T, int k, int E, int R, int capacity,
                          int32_t* rank_send_displs, void* ws, int32_t* status,
                          cudaStream_t stream) {
   const int64_t P = static_cast<int64_t>(T) * k;
+  if (P <= kSmallP && E <= kSmallE) {
+    const size_t smem = static_cast<size_t>(kSmallWarps + 2) * E * sizeof(int32_t);
+    layout_small_kernel<<<1, kSmallWarps * 32, smem, stream>>>(
+        P, E, R, capacity, topk_idx, expert_counts, expert_offsets, dst_row,
+        src_pair, n_kept, n_dropped, rank_send_counts, rank_send_displs,
+        status);
+    return launch_status();
+  }
   const int nchunks = static_cast<int>(ceil_div(P, kLayoutChunk));
   int32_t* w = static_cast<int32_t*>(ws);
   if (nchunks > 0)

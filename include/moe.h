@@ -141,6 +141,12 @@ MOE_API moe_status moe_route(const moe_route_cfg* cfg, const void* x, const void
  * histograms).  Returns 0 for invalid sizes. */
 MOE_API size_t moe_dispatch_layout_workspace_size(int32_t T, int32_t k, int32_t E);
 
+/* Kernels one moe_dispatch_layout (or moe_dispatch_layout_noalloc) call
+ * launches: 1 when one block does the whole layout (T*k <= 16384 pairs and
+ * E <= 256), else 3 (histogram, scan, assignment; 1 for T = 0); 0 for
+ * invalid sizes.  Host only. */
+MOE_API int32_t moe_dispatch_layout_launches(int32_t T, int32_t k, int32_t E);
+
 /* moe_dispatch_layout -- binning of the T*k (token, expert) pairs into an
  * expert-contiguous buffer ("Expert Parallelism in LLMs", The Execution
  * Pipeline, step 2 "Local Token Permutation"; "All-to-All Communication",

@@ -96,6 +96,17 @@ def test_layout_rejects_bad_sizes(lib):
     assert lib.moe_dispatch_layout(10, 2, 8, 4, 0, *nul) == L.MOE_ERR_INVALID
 
 
+def test_layout_launches(lib):
+    # one block up to 16384 pairs and 256 experts, else three kernels
+    assert lib.moe_dispatch_layout_launches(2048, 2, 8) == 1
+    assert lib.moe_dispatch_layout_launches(16384, 1, 64) == 1
+    assert lib.moe_dispatch_layout_launches(4096, 8, 128) == 3
+    assert lib.moe_dispatch_layout_launches(1000, 2, 300) == 3
+    assert lib.moe_dispatch_layout_launches(0, 2, 300) == 1
+    assert lib.moe_dispatch_layout_launches(16, 33, 8) == 0
+    assert lib.moe_dispatch_layout_launches(16, 2, 2000) == 0
+
+
 def test_permute_combine_reject(lib):
     assert lib.moe_permute(10, 2, 12, L.MOE_BF16, FAKE, FAKE, FAKE, None) == \
         L.MOE_ERR_INVALID                              # 24-byte rows

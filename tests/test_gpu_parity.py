@@ -118,6 +118,9 @@ LAYOUT_CASES = [
     (1500, 3, 1024, 32, 2, "dup"), (65536, 8, 128, 8, 0, "distinct"),
     # more than 256 chunks of 2048 pairs: the scan takes several batches
     (70000, 8, 64, 8, 0, "dup"),
+    # either side of the one-block layout (<= 16384 pairs, <= 256 experts)
+    (2048, 8, 256, 8, 30, "skew"), (2049, 8, 64, 8, 0, "dup"),
+    (2000, 2, 260, 4, 0, "dup"), (4096, 8, 256, 8, 60, "skew"),
 ]
 
 
