@@ -11,8 +11,11 @@
 //           fp32 accumulation in slot order (deterministic, no atomics),
 //           traffic N*D*s read + T*D*s written.
 //
-// One warp per token; each lane moves 16-byte vectors.  Up to 4 vectors
-// per lane are in flight per step for memory-level parallelism.
+// One warp per (token, row segment); each lane moves 16-byte vectors, up
+// to 4 in flight per step for memory-level parallelism.  A row is one
+// segment unless there are too few tokens to keep HBM busy: then it is cut
+// into up to 4 segments of at least 128 vectors, each its own warp (for
+// combine only with k <= 4).
 #include "common.cuh"
 #include "internal.h"
 
@@ -23,21 +26,26 @@ constexpr int kUnroll = 4;     // 16-byte vectors per lane per step
 
 template <typename T>
 __global__ void __launch_bounds__(kRowWarps * 32)
-    permute_kernel(int64_t n_tok, int k, int nvec, const uint4* __restrict__ x,
+    permute_kernel(int64_t n_tok, int k, int nvec, int nseg,
+                   const uint4* __restrict__ x,
                    const int32_t* __restrict__ dst_row, uint4* __restrict__ xp) {
   const int lane = threadIdx.x & 31;
   const int64_t warp_g = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kRowWarps;
-  for (int64_t t = warp_g; t < n_tok; t += nwarps) {
+  const int segv = nvec / nseg;
+  for (int64_t u = warp_g; u < n_tok * nseg; u += nwarps) {
+    const int64_t t = u / nseg;
+    const int v_begin = static_cast<int>(u - t * nseg) * segv;
+    const int v_end = v_begin + segv;
     // lane j < k holds the destination row of slot j
     const int32_t my_dst = lane < k ? __ldg(dst_row + t * k + lane) : -1;
     const uint4* src = x + t * nvec;
-    for (int v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
+    for (int v0 = v_begin + lane; v0 < v_end; v0 += 32 * kUnroll) {
       uint4 buf[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int v = v0 + u * 32;
-        if (v < nvec) buf[u] = ld_nc_v4(src + v);
+        if (v < v_end) buf[u] = ld_nc_v4(src + v);
       }
       for (int j = 0; j < k; ++j) {
         const int32_t r = __shfl_sync(0xffffffffu, my_dst, j);
@@ -46,30 +54,38 @@ __global__ void __launch_bounds__(kRowWarps * 32)
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int v = v0 + u * 32;
-          if (v < nvec) st_v4(dst + v, buf[u]);
+          if (v < v_end) st_v4(dst + v, buf[u]);
         }
       }
     }
   }
 }
 
-template <typename T>
+// SEG = false is the one-segment case with the segment arithmetic folded
+// away (measured faster than the general loop run with nseg = 1).
+template <typename T, bool SEG>
 __global__ void __launch_bounds__(kRowWarps * 32)
-    combine_kernel(int64_t n_tok, int k, int nvec, const uint4* __restrict__ yp,
+    combine_kernel(int64_t n_tok, int k, int nvec, int nseg_arg,
+                   const uint4* __restrict__ yp,
                    const int32_t* __restrict__ dst_row,
                    const float* __restrict__ gate, uint4* __restrict__ y) {
   constexpr int N = Vec16<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t warp_g = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kRowWarps;
-  for (int64_t t = warp_g; t < n_tok; t += nwarps) {
+  const int nseg = SEG ? nseg_arg : 1;
+  const int segv = nvec / nseg;
+  for (int64_t u = warp_g; u < n_tok * nseg; u += nwarps) {
+    const int64_t t = u / nseg;
+    const int v_begin = static_cast<int>(u - t * nseg) * segv;
+    const int v_end = v_begin + segv;
     const int32_t my_dst = lane < k ? __ldg(dst_row + t * k + lane) : -1;
     // gate == nullptr: unit gates (the permute backward sums the rows)
     const float my_g =
         lane < k ? (gate != nullptr ? __ldg(gate + t * k + lane) : 1.0f)
                  : 0.0f;
     uint4* out = y + t * nvec;
-    for (int v0 = lane; v0 < nvec; v0 += 32 * kUnroll) {
+    for (int v0 = v_begin + lane; v0 < v_end; v0 += 32 * kUnroll) {
       float acc[kUnroll][N];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u)
@@ -84,7 +100,7 @@ __global__ void __launch_bounds__(kRowWarps * 32)
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int v = v0 + u * 32;
-          if (v < nvec) buf[u] = ld_nc_v4(src + v);
+          if (v < v_end) buf[u] = ld_nc_v4(src + v);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -97,15 +113,26 @@ __global__ void __launch_bounds__(kRowWarps * 32)
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int v = v0 + u * 32;
-        if (v < nvec) st_v4(out + v, Vec16<T>::from_f32(acc[u]));
+        if (v < v_end) st_v4(out + v, Vec16<T>::from_f32(acc[u]));
       }
     }
   }
 }
 
-static unsigned row_grid(int64_t T, int num_sms) {
+// Segments per row: double while the warps would number fewer than 48 per
+// SM and each segment keeps at least 128 vectors (one full step of 32 lanes
+// x 4); a segment count always divides nvec.
+static int row_segments(int64_t T, int nvec, int num_sms) {
+  int nseg = 1;
+  while (nseg < 4 && T * nseg < static_cast<int64_t>(num_sms) * 48 &&
+         nvec % (2 * nseg) == 0 && nvec / (2 * nseg) >= 32 * kUnroll)
+    nseg *= 2;
+  return nseg;
+}
+
+static unsigned row_grid(int64_t units, int num_sms) {
   // enough resident warps to cover HBM latency: 8 blocks of 8 warps per SM
-  const int64_t want = ceil_div(T, kRowWarps);
+  const int64_t want = ceil_div(units, kRowWarps);
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   return static_cast<unsigned>(want < cap ? want : cap);
 }
@@ -115,14 +142,15 @@ moe_status launch_permute(int T, int k, int D, int dtype, const void* x,
                           cudaStream_t stream, int num_sms) {
   if (T == 0) return MOE_OK;
   const int nvec = static_cast<int>(D * dtype_bytes(dtype) / 16);
-  const unsigned grid = row_grid(T, num_sms);
+  const int nseg = row_segments(T, nvec, num_sms);
+  const unsigned grid = row_grid(static_cast<int64_t>(T) * nseg, num_sms);
   if (dtype == MOE_BF16)
     permute_kernel<__nv_bfloat16><<<grid, kRowWarps * 32, 0, stream>>>(
-        T, k, nvec, static_cast<const uint4*>(x), dst_row,
+        T, k, nvec, nseg, static_cast<const uint4*>(x), dst_row,
         static_cast<uint4*>(xp));
   else
     permute_kernel<float><<<grid, kRowWarps * 32, 0, stream>>>(
-        T, k, nvec, static_cast<const uint4*>(x), dst_row,
+        T, k, nvec, nseg, static_cast<const uint4*>(x), dst_row,
         static_cast<uint4*>(xp));
   return launch_status();
 }
@@ -132,15 +160,27 @@ moe_status launch_combine(int T, int k, int D, int dtype, const void* yp,
                           cudaStream_t stream, int num_sms) {
   if (T == 0) return MOE_OK;
   const int nvec = static_cast<int>(D * dtype_bytes(dtype) / 16);
-  const unsigned grid = row_grid(T, num_sms);
-  if (dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<grid, kRowWarps * 32, 0, stream>>>(
-        T, k, nvec, static_cast<const uint4*>(yp), dst_row, gate,
-        static_cast<uint4*>(y));
-  else
-    combine_kernel<float><<<grid, kRowWarps * 32, 0, stream>>>(
-        T, k, nvec, static_cast<const uint4*>(yp), dst_row, gate,
-        static_cast<uint4*>(y));
+  // with more than 4 slots a token's gather already has enough independent
+  // loads; splitting its row measured slower (k = 8)
+  const int nseg = k <= 4 ? row_segments(T, nvec, num_sms) : 1;
+  const unsigned grid = row_grid(static_cast<int64_t>(T) * nseg, num_sms);
+  const uint4* src = static_cast<const uint4*>(yp);
+  uint4* dst = static_cast<uint4*>(y);
+  if (dtype == MOE_BF16) {
+    if (nseg > 1)
+      combine_kernel<__nv_bfloat16, true><<<grid, kRowWarps * 32, 0, stream>>>(
+          T, k, nvec, nseg, src, dst_row, gate, dst);
+    else
+      combine_kernel<__nv_bfloat16, false><<<grid, kRowWarps * 32, 0, stream>>>(
+          T, k, nvec, 1, src, dst_row, gate, dst);
+  } else {
+    if (nseg > 1)
+      combine_kernel<float, true><<<grid, kRowWarps * 32, 0, stream>>>(
+          T, k, nvec, nseg, src, dst_row, gate, dst);
+    else
+      combine_kernel<float, false><<<grid, kRowWarps * 32, 0, stream>>>(
+          T, k, nvec, 1, src, dst_row, gate, dst);
+  }
   return launch_status();
 }
 

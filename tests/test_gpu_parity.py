@@ -305,7 +305,9 @@ def test_sigmoid_key_bit_exact():
 @pytest.mark.parametrize("T,k,E,D,dt,cap", [
     (1, 1, 4, 8, torch.bfloat16, 0), (37, 2, 8, 64, torch.bfloat16, 0),
     (300, 8, 16, 520, torch.bfloat16, 30), (129, 2, 8, 64, torch.float32, 20),
-    (2048, 8, 128, 4096, torch.bfloat16, 0)])
+    (2048, 8, 128, 4096, torch.bfloat16, 0),
+    # rows cut into 2 segments of 192 vectors, and into 4 with drops
+    (777, 2, 8, 3072, torch.bfloat16, 0), (500, 2, 8, 2048, torch.float32, 40)])
 def test_permute_combine_parity(T, k, E, D, dt, cap):
     idx = _idx("distinct", T, k, E, seed=D)
     lay = O.dispatch_layout(idx, E, 1, cap if cap > 0 else None)
