@@ -202,14 +202,3 @@ def draw_routing(T, E, k, kind, zipf_s, gen, device):
     ex = -torch.log(ex.clamp_min(1e-300))
     gate = (ex / ex.sum(dim=1, keepdim=True)).to(torch.float32)
     return idx.contiguous(), gate.contiguous()
-
-
-def random_topk_idx(T, E, k, seed, device="cpu", distinct=True):
-    """Plain random expert ids [T, k] int32 (distinct per token when asked),
-    for layout-only tests."""
-    g = _gen(seed, 9, device)
-    if distinct:
-        keys = torch.rand((T, E), generator=g, device=device)
-        return torch.topk(keys, k, dim=1).indices.to(torch.int32).contiguous()
-    return torch.randint(0, E, (T, k), generator=g, device=device,
-                         dtype=torch.int32)

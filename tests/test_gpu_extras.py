@@ -341,6 +341,12 @@ def test_host_stream_matches_forward_bitwise():
         ref = layer.forward(xh.to(DEV)).cpu()
         torch.cuda.synchronize()
         assert torch.equal(yh, ref)
+    # the single-batch form: copy in, run, copy out on one stream
+    x_dev = torch.empty((wl.T, wl.D), dtype=torch.bfloat16, device=DEV)
+    y1 = torch.full((wl.T, wl.D), float("nan"), dtype=torch.bfloat16).pin_memory()
+    layer.forward_host(xs[2], y1, x_dev)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, ys[2])
     assert layer.device_status() == 0
 
 
