@@ -133,6 +133,17 @@ def test_layout_bit_exact(T, k, E, R, cap, kind):
     assert int(g["status"][0]) == 0
 
 
+@pytest.mark.parametrize("E,R,cap", [(8, 4, 0), (300, 4, 5)])
+def test_layout_empty_batch(E, R, cap):
+    # T = 0: every count, offset, rank count and displacement is 0 (the
+    # one-block path for E = 8, the three-launch path for E = 300)
+    idx = np.zeros((0, 2), dtype=np.int32)
+    g = run_layout(idx, E, R, cap)
+    ref = O.dispatch_layout(idx, E, R, cap or None)
+    check_layout(g, ref, 0)
+    assert int(g["status"][0]) == 0
+
+
 def test_layout_page_worked_example():
     idx = np.array([[0, 2], [1, 3], [0, 1], [2, 3]], dtype=np.int32)
     g = run_layout(idx, 4, 2, 0)
@@ -396,6 +407,38 @@ def test_grouped_ffn_parity(case):
     assert np.isfinite(got).all()
     assert rel_err(got, ref) <= tol_for(dt)
     assert torch.isnan(yp[n:].float()).all()
+
+
+def test_grouped_ffn_all_experts_empty():
+    # offsets all zero: no tile runs and the output rows stay untouched
+    E, D, F, max_rows = 4, 128, 256, 64
+    g = torch.Generator().manual_seed(5)
+    xp = torch.randn((max_rows, D), generator=g).to(torch.bfloat16)
+    w13 = (torch.randn((E, 2 * F, D), generator=g) * 0.05).to(torch.bfloat16)
+    w2 = (torch.randn((E, D, F), generator=g) * 0.05).to(torch.bfloat16)
+    yp, _ = run_ffn(xp, [0] * E, w13, w2, F)
+    assert torch.isnan(yp.float()).all()
+
+
+def test_empty_batch_through_every_call():
+    # T = 0 through route, permute and combine: each returns MOE_OK and
+    # launches nothing (the C ABI raises on any other status)
+    D, E, k = 256, 8, 2
+    cfg = L.route_cfg(0, D, E, k, torch.bfloat16, "softmax_topk")
+    x = torch.empty((0, D), dtype=torch.bfloat16, device=DEV)
+    w = torch.randn((E, D), device=DEV).to(torch.bfloat16)
+    ws = torch.empty(max(L.moe_route_workspace_size(cfg), 16),
+                     dtype=torch.uint8, device=DEV)
+    idx = torch.empty((0, k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((0, k), dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.moe_route(cfg, x, w, None, None, idx, gate, None, ws, st)
+    dst = torch.empty((0,), dtype=torch.int32, device=DEV)
+    xp = torch.empty((0, D), dtype=torch.bfloat16, device=DEV)
+    L.moe_permute(0, k, D, L.MOE_BF16, x, dst, xp)
+    L.moe_combine(0, k, D, L.MOE_BF16, xp, dst, gate, x)
+    torch.cuda.synchronize()
+    assert st.item() == 0
 
 
 # ------------------------------------------------------------ whole layer
