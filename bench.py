@@ -71,9 +71,10 @@ def capture_stages(stages, dev):
 K_graph_cap = 200
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from ncu, keyed by
-# (workload, T, step): the grouped FFN's up (1.9366 GB + 113.1 MB) and down
-# (1.1282 GB + 28.9 MB) launches of the Mixtral-like layer.
-NCU_DRAM_BYTES = {("mixtral_bf16", 2048, "ffn"): 3.2068e9}
+# (workload, T, step): the grouped FFN's up (1.9369 GB + 112.3 MB) and down
+# (1.1284 GB + 25.0 MB) launches of the Mixtral-like layer, taken on the
+# current kernels.
+NCU_DRAM_BYTES = {("mixtral_bf16", 2048, "ffn"): 3.2026e9}
 
 # tokens of the bounded CPU-oracle sample, per workload (about 10-30 s of
 # host work)
