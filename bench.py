@@ -384,9 +384,8 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
                 "traffic": None, "peak_note": "HBM copy, " + peaks["source"],
                 "algorithmic_per_launch": dm["bytes"]}
     # DRAM bytes (read + write) of one launch of the dominant kernel, from an
-    # ncu capture of the same kernel on the same workload
-    # (profiles/ffn_umma_mixtral_T2048_full.md); re-take it when the kernel
-    # changes.
+    # ncu capture of the same kernel on the same workload; re-take it when
+    # the kernel changes.
     dram = NCU_DRAM_BYTES.get((wl.name, wl.T, dom))
     if dram is not None:
         roof["traffic"] = dram
