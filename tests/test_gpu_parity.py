@@ -3,7 +3,7 @@ against the CPU oracle on the same seeded inputs.
 
 Bars (written into each check):
   * integers (top-k ids, counts, offsets, dst_row, src_pair, rank counts):
-    bit-exact; routing ids are judged on the logits the kernel used
+    bit-exact; routing ids are checked on the logits the kernel used
     (logits_out), so both sides take the selection on the same fp32 values;
   * gates: |g - g_ref| <= 2e-6;
   * router logits: |l - l_ref| <= 2^-16 * sum_d |x_d w_d| + 1e-6 (fp32
