@@ -313,6 +313,14 @@ RoutePlan plan_route(const moe_route_cfg& c, int num_sms) {
     // enough (m block, K split) tiles to cover the SMs, >= 4 K blocks each
     splits = num_sms / (m_tiles > 0 ? m_tiles : 1);
     splits = splits < 1 ? 1 : splits;
+    // with more row blocks than SMs, two K halves when they even out the
+    // last round by at least half a tile (512 blocks on 148 SMs: 3.5
+    // tile-times instead of 4)
+    if (m_tiles >= num_sms) {
+      const int64_t whole = ceil_div(m_tiles, num_sms);
+      const int64_t halves = ceil_div(2 * static_cast<int64_t>(m_tiles), num_sms);
+      if (halves <= 2 * whole - 1) splits = 2;
+    }
     const int max_splits = p.k_blocks / 4 > 0 ? p.k_blocks / 4 : 1;
     splits = splits > max_splits ? max_splits : splits;
   }

@@ -252,6 +252,8 @@ ROUTE_CASES = [
     (12000, 64, 8, 2, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
     (20000, 128, 200, 5, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
     (10000, 128, 64, 9, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
+    # more row blocks than SMs, unevenly: the GEMM runs as two K halves
+    (20000, 512, 64, 4, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
     (10000, 128, 64, 4, torch.bfloat16, "softmax_topk", (4, 2, 2), None, None, None),
 ]
 
