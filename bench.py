@@ -71,10 +71,10 @@ def capture_stages(stages, dev):
 K_graph_cap = 200
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from ncu, keyed by
-# (workload, T, step): the grouped FFN's up (1.9369 GB + 112.3 MB) and down
-# (1.1284 GB + 25.0 MB) launches of the Mixtral-like layer, taken on the
-# current kernels.
-NCU_DRAM_BYTES = {("mixtral_bf16", 2048, "ffn"): 3.2026e9}
+# (workload, T, step): the grouped FFN's one launch (up and down projection)
+# on the Mixtral-like layer, 3.0816 GB read + 145.4 MB written, taken on the
+# current kernel.
+NCU_DRAM_BYTES = {("mixtral_bf16", 2048, "ffn"): 3.2270e9}
 
 # tokens of the bounded CPU-oracle sample, per workload (about 10-30 s of
 # host work)
@@ -176,7 +176,7 @@ def launches_per_step(layer, routed):
     if routed:
         n += 2                   # route: router GEMM + select
     if not layer.identity:
-        n += 2                   # grouped FFN: up and down projections
+        n += 1                   # grouped FFN: up and down in one launch
     return n
 
 
@@ -392,7 +392,7 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
         roof["traffic_over_algorithmic"] = round(
             dram / (dm["bytes"] if dk["bound"] == "hbm" else
                     models[dom]["bytes"]), 3)
-    roof["kernel"] = {"ffn": "moe_grouped_ffn (tcgen05 up + down launches)",
+    roof["kernel"] = {"ffn": "moe_grouped_ffn (one tcgen05 launch, up + down)",
                       "route": "moe_route (router GEMM + select)",
                       "layout": "moe_dispatch_layout (3 launches)",
                       "permute": "moe_permute", "combine": "moe_combine"}[dom]

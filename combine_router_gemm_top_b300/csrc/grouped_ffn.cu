@@ -16,6 +16,7 @@
 // fp32: plain FMA kernels, one thread per output element.
 #include "common.cuh"
 #include "internal.h"
+#include "umma_ffn.cuh"
 #include "umma_gemm.cuh"
 
 namespace moe {
@@ -71,11 +72,24 @@ __global__ void ffn_down_f32_kernel(int E, int D, int F, int max_rows,
 }
 
 // ----------------------------------------------------------- host
-size_t ffn_ws_bytes(int E, int D, int F, int max_rows, int dtype) {
-  (void)E;
-  (void)D;
-  return static_cast<size_t>(max_rows) * F * dtype_bytes(dtype);
+// Workspace: H [max_rows, F], then (bf16) one ready counter per row block of
+// the fused launch: at most ceil(max_rows / 128) + E blocks.
+static size_t ffn_h_bytes(int F, int max_rows, int dtype) {
+  return (static_cast<size_t>(max_rows) * F * dtype_bytes(dtype) + 255) &
+         ~size_t(255);
 }
+static int ffn_ready_cap(int E, int max_rows) {
+  return static_cast<int>(ceil_div(max_rows, kBM)) + E;
+}
+
+size_t ffn_ws_bytes(int E, int D, int F, int max_rows, int dtype) {
+  (void)D;
+  if (dtype != MOE_BF16)
+    return static_cast<size_t>(max_rows) * F * dtype_bytes(dtype);
+  return ffn_h_bytes(F, max_rows, dtype) +
+         static_cast<size_t>(ffn_ready_cap(E, max_rows)) * sizeof(uint32_t);
+}
+
 
 moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
                               const void* xp, const int32_t* offsets,
@@ -121,8 +135,6 @@ moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
   up.out_cols = F;
   up.status = status;
   up.wait_limit_ns = kWaitLimitNs;
-  moe_status s = launch_umma<kUp>(tm_xp, tm_w13, up, stream, num_sms);
-  if (s != MOE_OK) return s;
 
   GemmArgs dn = up;
   dn.k_blocks = F / kBK;
@@ -132,7 +144,26 @@ moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
   dn.out = yp;
   dn.out_ld = D;
   dn.out_cols = D;
-  return launch_umma<kDown>(tm_h, tm_w2, dn, stream, num_sms);
+
+  // up and down projection in one persistent launch (umma_ffn.cuh)
+  FfnArgs f{};
+  f.up = up;
+  f.dn = dn;
+  f.ready = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) +
+                                        ffn_h_bytes(F, max_rows, dtype));
+  f.ready_cap = ffn_ready_cap(E, max_rows);
+  if (cudaMemsetAsync(f.ready, 0, static_cast<size_t>(f.ready_cap) *
+                                      sizeof(uint32_t),
+                      stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  static std::atomic<uint64_t> attr_done{0};
+  if (!set_smem_limit_once(reinterpret_cast<const void*>(umma_ffn_kernel),
+                           227 * 1024, &attr_done))
+    return MOE_ERR_CUDA;
+  const size_t smem = umma_gemm_smem_bytes(up.BN, up.stages);
+  umma_ffn_kernel<<<num_sms, kGemmThreads, smem, stream>>>(tm_xp, tm_w13, tm_h,
+                                                          tm_w2, f);
+  return launch_status();
 }
 
 // ----------------------------------------------------------- self-test

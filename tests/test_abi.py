@@ -140,8 +140,11 @@ def test_grouped_ffn_reject(lib):
     assert lib.moe_grouped_ffn(8, 128, 256, 64, L.MOE_BF16, FAKE, None, FAKE,
                                FAKE, FAKE, FAKE, ok_ws, None, None) == \
         L.MOE_ERR_INVALID
+    # H [max_rows, F], then one counter per row block (ceil(64/128) + E)
     assert lib.moe_grouped_ffn_workspace_size(8, 128, 256, 64, L.MOE_BF16) == \
-        64 * 256 * 2
+        64 * 256 * 2 + (1 + 8) * 4
+    assert lib.moe_grouped_ffn_workspace_size(8, 128, 256, 64, L.MOE_F32) == \
+        64 * 256 * 4
 
 
 def test_route_backward_reject(lib):
