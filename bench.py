@@ -174,7 +174,9 @@ def launches_per_step(layer, routed):
     # layout (one block, or histogram + scan + assignment), permute, combine
     n = L.moe_dispatch_layout_launches(layer.T, layer.k, layer.E) + 1 + 1
     if routed:
-        n += 2                   # route: router GEMM + select
+        # route: one warp-per-token kernel up to 32 experts, else the router
+        # GEMM and the select kernel
+        n += L.moe_route_launches(layer.cfg)
     if not layer.identity:
         n += 1                   # grouped FFN: up and down in one launch
     return n

@@ -33,7 +33,7 @@ SCORE_CODES = {"softmax_topk": MOE_SCORE_SOFTMAX_TOPK,
                "softmax_full": MOE_SCORE_SOFTMAX_FULL,
                "sigmoid_bias": MOE_SCORE_SIGMOID_BIAS}
 
-EXPORTED = ["moe_route_workspace_size", "moe_route",
+EXPORTED = ["moe_route_workspace_size", "moe_route_launches", "moe_route",
             "moe_dispatch_layout_workspace_size",
             "moe_dispatch_layout_launches", "moe_dispatch_layout",
             "moe_permute", "moe_grouped_ffn_workspace_size",
@@ -71,6 +71,7 @@ _u64 = ctypes.c_uint64
 
 _SIGS = {
     "moe_route_workspace_size": (_sz, [ctypes.POINTER(RouteCfg)]),
+    "moe_route_launches": (_i32, [ctypes.POINTER(RouteCfg)]),
     "moe_route": (_i32, [ctypes.POINTER(RouteCfg), _vp, _vp, _vp, _vp, _vp,
                          _vp, _vp, _vp, _sz, _vp, _vp]),
     "moe_dispatch_layout_workspace_size": (_sz, [_i32, _i32, _i32]),
@@ -184,6 +185,10 @@ def route_cfg(T, D, E, k, dtype, score, n_groups=1, topk_groups=1,
 
 def moe_route_workspace_size(cfg: RouteCfg) -> int:
     return load().moe_route_workspace_size(ctypes.byref(cfg))
+
+
+def moe_route_launches(cfg: RouteCfg) -> int:
+    return load().moe_route_launches(ctypes.byref(cfg))
 
 
 def moe_route(cfg, x, w_r, logit_offset, sel_bias, topk_idx, topk_gate,

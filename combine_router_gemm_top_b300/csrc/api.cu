@@ -116,6 +116,11 @@ size_t moe_route_workspace_size(const moe_route_cfg* cfg) {
   return b > 0 ? b : 16;
 }
 
+int32_t moe_route_launches(const moe_route_cfg* cfg) {
+  if (!route_cfg_ok(cfg) || cfg->T == 0) return 0;
+  return route_single_kernel(*cfg) ? 1 : 2;
+}
+
 moe_status moe_route(const moe_route_cfg* cfg, const void* x, const void* w_r,
                      const float* logit_offset, const float* sel_bias,
                      int32_t* topk_idx, float* topk_gate, float* logits_out,

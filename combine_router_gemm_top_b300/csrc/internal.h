@@ -29,6 +29,7 @@ struct RoutePlan {
   size_t ws_bytes;   // partial logits [splits][T][E] fp32
 };
 RoutePlan plan_route(const moe_route_cfg& c, int num_sms);
+bool route_single_kernel(const moe_route_cfg& c);
 
 struct RouteSelectArgs {
   int T, E, k, score, n_groups, topk_groups, group_score_topk, splits;
@@ -38,6 +39,7 @@ struct RouteSelectArgs {
   int32_t* topk_idx;
   float* topk_gate;
   float* logits_out;
+  int32_t* status;  // receives MOE_ERR_TIMEOUT if a bounded wait expires
 };
 
 moe_status launch_route(const moe_route_cfg& c, const void* x, const void* w_r,

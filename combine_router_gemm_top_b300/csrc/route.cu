@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <float.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 #include "umma_gemm.cuh"
@@ -98,40 +100,14 @@ __device__ __forceinline__ int group_of(int e, float inv_gs) {
 constexpr int kSelWarps = 8;
 constexpr int kSelGroupTop = 8;   // per-lane scan handles group_score_topk <= 8
 
-// One warp per token; lane l holds experts e = l + 32*i, i < NI.
+// Selection for one token, one warp: lane l holds the logits of experts
+// e = l + 32*i, i < NI, in lg; sk is the warp's shared scratch for the
+// group scan.  Writes the token's ids and gates (and logits when asked).
 template <int NI>
-__global__ void __launch_bounds__(kSelWarps * 32)
-    route_select_kernel(RouteSelectArgs a) {
-  // keys of each warp's token for the group scan, one pad word per 32 so
-  // that lanes reading along different groups hit different banks
-  __shared__ float skey[kSelWarps][256 + 8];
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kSelWarps + warp;
-  if (t >= a.T) return;
+__device__ __forceinline__ void select_token(const RouteSelectArgs& a,
+                                             int64_t t, int lane,
+                                             float (&lg)[NI], float* sk) {
   const int E = a.E;
-
-  // split-K partial sums added in split order; the loads of one split are
-  // independent of each other
-  float lg[NI];
-#pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    const int e = lane + 32 * i;
-    lg[i] = e < E ? a.partial[t * E + e] : 0.0f;
-  }
-#pragma unroll 2
-  for (int s = 1; s < a.splits; ++s) {
-    const float* ps = a.partial + (static_cast<int64_t>(s) * a.T + t) * E;
-    float p[NI];
-#pragma unroll
-    for (int i = 0; i < NI; ++i) {
-      const int e = lane + 32 * i;
-      p[i] = e < E ? ps[e] : 0.0f;
-    }
-#pragma unroll
-    for (int i = 0; i < NI; ++i) lg[i] = __fadd_rn(lg[i], p[i]);
-  }
-
   float key[NI];
   uint32_t code[NI];
 #pragma unroll
@@ -164,7 +140,6 @@ __global__ void __launch_bounds__(kSelWarps * 32)
     if (m <= kSelGroupTop) {
       // lane g scans its group's keys, keeping the m largest in a sorted
       // list; equal keys are interchangeable for the sum
-      float* sk = skey[warp];
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
         const int e = lane + 32 * i;
@@ -275,6 +250,139 @@ __global__ void __launch_bounds__(kSelWarps * 32)
   }
 }
 
+// One warp per token: the split-K partial sums, added in split order (the
+// loads of one split are independent of each other), then the selection.
+template <int NI>
+__global__ void __launch_bounds__(kSelWarps * 32)
+    route_select_kernel(RouteSelectArgs a) {
+  // keys of each warp's token for the group scan, one pad word per 32 so
+  // that lanes reading along different groups hit different banks
+  __shared__ float skey[kSelWarps][256 + 8];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kSelWarps + warp;
+  if (t >= a.T) return;
+  const int E = a.E;
+  float lg[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int e = lane + 32 * i;
+    lg[i] = e < E ? a.partial[t * E + e] : 0.0f;
+  }
+#pragma unroll 2
+  for (int s = 1; s < a.splits; ++s) {
+    const float* ps = a.partial + (static_cast<int64_t>(s) * a.T + t) * E;
+    float p[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int e = lane + 32 * i;
+      p[i] = e < E ? ps[e] : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < NI; ++i) lg[i] = __fadd_rn(lg[i], p[i]);
+  }
+  select_token<NI>(a, t, lane, lg, skey[warp]);
+}
+
+// The whole router for small E x D in one kernel, one warp per token.  One
+// thread copies W_r (E x D) into shared memory with a single bulk copy while
+// the warps' first x vectors are in flight; rows E..EP-1 are zero so that the
+// expert loop has no branch.  Lane l owns the token's 16-byte vectors l,
+// l + 32, ..., accumulates the EP dot products in fp32 on the FMA pipes, a
+// shuffle tree adds the lanes' parts, and lane e keeps expert e's logit for
+// the selection.  For few experts this replaces a tensor-core GEMM split many
+// ways plus a separate select launch.
+template <typename T, int EP>
+__global__ void __launch_bounds__(kSelWarps * 32)
+    route_warp_kernel(RouteSelectArgs a, const T* __restrict__ x,
+                      const T* __restrict__ w, int D) {
+  extern __shared__ __align__(16) uint4 wsm[];  // [EP][D / N] 16-byte vectors
+  __shared__ float skey[kSelWarps][256 + 8];
+  __shared__ uint64_t wbar;
+  __shared__ int abort_flag;
+  constexpr int N = Vec16<T>::N;
+  constexpr int U = EP <= 8 ? 8 : 4;  // vectors a lane loads per batch; two batches in flight
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kSelWarps + warp;
+  const bool active = t < a.T;
+  const int E = a.E;
+  const int nvec = D / N;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&wbar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t bytes = static_cast<uint32_t>(E) * nvec * 16u;
+    mbar_arrive_expect_tx(&wbar, bytes);
+    bulk_load_g2s(wsm, w, bytes, &wbar);
+  }
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (active ? t : 0) * D);
+  uint4 xv[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int v = lane + 32 * u;
+    xv[u] = active && v < nvec ? ld_nc_v4(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  for (int i = E * nvec + threadIdx.x; i < EP * nvec; i += kSelWarps * 32)
+    wsm[i] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  if (!mbar_wait(&wbar, 0, &abort_flag, kWaitLimitNs)) {
+    if (threadIdx.x == 0) set_status(a.status, MOE_ERR_TIMEOUT);
+    return;
+  }
+  if (!active) return;
+  float acc[EP];
+#pragma unroll
+  for (int e = 0; e < EP; ++e) acc[e] = 0.0f;
+  for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+    uint4 cur[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      cur[u] = xv[u];
+      const int v = v0 + 32 * (U + u);
+      xv[u] = v < nvec ? ld_nc_v4(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u;
+      if (v < nvec) {
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+          const uint32_t xw[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
+#pragma unroll
+          for (int e = 0; e < EP; ++e) {
+            const uint4 wv = wsm[e * nvec + v];
+            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[e] = fma_bf16x2_f32(xw[i], ww[i], acc[e]);
+          }
+        } else {
+          float xf[N];
+          Vec16<T>::to_f32(cur[u], xf);
+#pragma unroll
+          for (int e = 0; e < EP; ++e) {
+            float wf[N];
+            Vec16<T>::to_f32(wsm[e * nvec + v], wf);
+#pragma unroll
+            for (int i = 0; i < N; ++i) acc[e] = fmaf(xf[i], wf[i], acc[e]);
+          }
+        }
+      }
+    }
+  }
+  float lg[1] = {0.0f};
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    float s = acc[e];
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d);
+    if (lane == e) lg[0] = s;
+  }
+  select_token<1>(a, t, lane, lg, skey[warp]);
+}
+
 // fp32 router GEMM on the FMA pipes: one thread per (token, expert).
 __global__ void route_gemm_f32_kernel(int T, int D, int E, const float* x,
                                       const float* w, float* logits) {
@@ -331,11 +439,67 @@ RoutePlan plan_route(const moe_route_cfg& c, int num_sms) {
   return p;
 }
 
+// Up to 32 experts, with W_r small enough to sit in shared memory, the router
+// is one warp-per-token kernel on the FMA pipes; otherwise the tensor-core
+// GEMM then the select kernel.
+constexpr int kWarpRouteSmem = 96 * 1024;
+static int route_ep(int E) { return E <= 8 ? 8 : E <= 16 ? 16 : 32; }
+bool route_single_kernel(const moe_route_cfg& c) {
+  return c.E <= 32 && static_cast<int64_t>(route_ep(c.E)) * c.D *
+                              dtype_bytes(c.dtype) <= kWarpRouteSmem;
+}
+
+template <typename T, int EP>
+static bool launch_route_warp_ep(const RouteSelectArgs& s, const T* x,
+                                 const T* w, int D, cudaStream_t stream) {
+  static std::atomic<uint64_t> attr_done{0};
+  if (!set_smem_limit_once(
+          reinterpret_cast<const void*>(route_warp_kernel<T, EP>),
+          kWarpRouteSmem, &attr_done))
+    return false;
+  const unsigned grid = static_cast<unsigned>(ceil_div(s.T, kSelWarps));
+  const size_t smem = static_cast<size_t>(EP) * D * sizeof(T);
+  route_warp_kernel<T, EP><<<grid, kSelWarps * 32, smem, stream>>>(s, x, w, D);
+  return true;
+}
+
+template <typename T>
+static bool launch_route_warp(const RouteSelectArgs& s, const void* x,
+                              const void* w_r, int D, cudaStream_t stream) {
+  const T* xx = static_cast<const T*>(x);
+  const T* ww = static_cast<const T*>(w_r);
+  if (s.E <= 8) return launch_route_warp_ep<T, 8>(s, xx, ww, D, stream);
+  if (s.E <= 16) return launch_route_warp_ep<T, 16>(s, xx, ww, D, stream);
+  return launch_route_warp_ep<T, 32>(s, xx, ww, D, stream);
+}
+
 moe_status launch_route(const moe_route_cfg& c, const void* x, const void* w_r,
                         const float* logit_offset, const float* sel_bias,
                         int32_t* topk_idx, float* topk_gate, float* logits_out,
                         void* ws, int32_t* status, cudaStream_t stream,
                         int num_sms) {
+  if (route_single_kernel(c)) {
+    RouteSelectArgs s{};
+    s.T = c.T;
+    s.E = c.E;
+    s.k = c.k;
+    s.score = c.score;
+    s.n_groups = c.n_groups;
+    s.topk_groups = c.topk_groups;
+    s.group_score_topk = c.group_score_topk;
+    s.splits = 1;
+    s.logit_offset = logit_offset;
+    s.sel_bias = sel_bias;
+    s.topk_idx = topk_idx;
+    s.topk_gate = topk_gate;
+    s.logits_out = logits_out;
+    s.status = status;
+    const bool ok = c.dtype == MOE_BF16
+                        ? launch_route_warp<__nv_bfloat16>(s, x, w_r, c.D, stream)
+                        : launch_route_warp<float>(s, x, w_r, c.D, stream);
+    if (!ok) return MOE_ERR_CUDA;
+    return launch_status();
+  }
   const RoutePlan p = plan_route(c, num_sms);
   float* partial = static_cast<float*>(ws);
   if (c.dtype == MOE_BF16) {

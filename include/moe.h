@@ -114,6 +114,13 @@ typedef struct {
  * split-K router GEMM).  Returns 0 for an invalid cfg. */
 MOE_API size_t moe_route_workspace_size(const moe_route_cfg* cfg);
 
+/* Kernels one moe_route call launches for `cfg`: 1 when E <= 32 and W_r,
+ * padded to 8, 16 or 32 rows, takes at most 96 KiB (one warp per token
+ * computes the logits on the CUDA cores from W_r in shared memory and
+ * selects), else 2 (the router GEMM, then the select kernel); 0 for an
+ * invalid cfg or T = 0.  Host only. */
+MOE_API int32_t moe_route_launches(const moe_route_cfg* cfg);
+
 /* moe_route -- router GEMM, score, top-k and gates
  * ("Expert Parallelism in LLMs", The Execution Pipeline, step 1 "Router
  *  Gating and Softmax Selection"; "All-to-All Communication", phase 1

@@ -96,6 +96,21 @@ def test_layout_rejects_bad_sizes(lib):
     assert lib.moe_dispatch_layout(10, 2, 8, 4, 0, *nul) == L.MOE_ERR_INVALID
 
 
+def test_route_launches(lib):
+    # one warp-per-token kernel up to 32 experts with E*D*elem <= 96 KiB
+    # (W_r in shared memory), else GEMM + select
+    for E, D, dt, n in [(8, 4096, L.MOE_BF16, 1), (32, 1024, L.MOE_BF16, 1),
+                        (32, 4096, L.MOE_BF16, 2), (33, 64, L.MOE_BF16, 2),
+                        (256, 4096, L.MOE_BF16, 2), (8, 3072, L.MOE_F32, 1),
+                        (8, 4096, L.MOE_F32, 2)]:
+        cfg = L.route_cfg(2048, D, E, 2, dt, 0)
+        assert lib.moe_route_launches(ctypes.byref(cfg)) == n, (E, D, dt)
+    assert lib.moe_route_launches(ctypes.byref(
+        L.route_cfg(0, 4096, 8, 2, L.MOE_BF16, 0))) == 0
+    assert lib.moe_route_launches(ctypes.byref(
+        L.route_cfg(128, 256, 8, 9, L.MOE_BF16, 0))) == 0
+
+
 def test_layout_launches(lib):
     # one block up to 16384 pairs and 256 experts, else three kernels
     assert lib.moe_dispatch_layout_launches(2048, 2, 8) == 1

@@ -239,6 +239,10 @@ ROUTE_CASES = [
     (64, 128, 4, 4, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
     (1, 64, 8, 1, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
     (513, 96, 24, 5, torch.float32, "sigmoid_bias", (3, 2, 2), None, None, 0.05),
+    # more than 32 experts in fp32: the FMA router GEMM, then the select kernel
+    (300, 64, 40, 3, torch.float32, "softmax_topk", (1, 1, 0), 0.02, None, None),
+    # 32 experts exactly: the one-kernel router at its widest
+    (700, 1024, 32, 4, torch.bfloat16, "softmax_full", (1, 1, 0), None, 1.5, None),
     # group scores over more than 8 keys (the warp-round path)
     (333, 128, 64, 6, torch.bfloat16, "sigmoid_bias", (4, 2, 12), None, None, 0.2),
     (300, 128, 96, 8, torch.bfloat16, "softmax_topk", (6, 3, 16), None, None, None),
