@@ -223,7 +223,9 @@ MOE_API moe_status moe_permute(int32_t T, int32_t k, int32_t D, int32_t dtype,
                        moe_stream_t stream);
 
 /* Bytes of scratch moe_grouped_ffn needs: the SwiGLU hidden activations
- * H [max_rows, F] in the compute dtype. */
+ * H [max_rows, F] in the compute dtype, then (bf16) one 32-bit counter per
+ * 128-row block (ceil(max_rows / 128) + E), which the call zeroes itself on
+ * the stream. */
 MOE_API size_t moe_grouped_ffn_workspace_size(int32_t E, int32_t D, int32_t F,
                                       int32_t max_rows, int32_t dtype);
 
