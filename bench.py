@@ -178,7 +178,9 @@ def launches_per_step(layer, routed):
         # GEMM and the select kernel
         n += L.moe_route_launches(layer.cfg)
     if not layer.identity:
-        n += 1                   # grouped FFN: up and down in one launch
+        # grouped FFN: bf16 up and down in one tcgen05 launch; fp32 as two
+        # CUDA-core kernels (up, down)
+        n += 1 if layer.dcode == L.MOE_BF16 else 2
     return n
 
 
@@ -394,10 +396,18 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
         roof["traffic_over_algorithmic"] = round(
             dram / (dm["bytes"] if dk["bound"] == "hbm" else
                     models[dom]["bytes"]), 3)
-    roof["kernel"] = {"ffn": "moe_grouped_ffn (one tcgen05 launch, up + down)",
-                      "route": "moe_route (router GEMM + select)",
-                      "layout": "moe_dispatch_layout (3 launches)",
-                      "permute": "moe_permute", "combine": "moe_combine"}[dom]
+    from combine_router_gemm_top_b300 import _lib as L
+    n_layout = L.moe_dispatch_layout_launches(layer.T, layer.k, layer.E)
+    roof["kernel"] = {
+        "ffn": ("moe_grouped_ffn (one tcgen05 launch, up + down)"
+                if layer.dcode == L.MOE_BF16 else
+                "moe_grouped_ffn (fp32: up and down kernels on CUDA cores)"),
+        "route": ("moe_route (one warp-per-token kernel)"
+                  if L.moe_route_launches(layer.cfg) == 1 else
+                  "moe_route (router GEMM + select)"),
+        "layout": f"moe_dispatch_layout ({n_layout} launch"
+                  f"{'es' if n_layout > 1 else ''})",
+        "permute": "moe_permute", "combine": "moe_combine"}[dom]
     pc_bytes = models["permute"]["bytes"] + models["combine"]["bytes"]
     pc_ms = (parts["permute"] + parts["combine"]) / K
     pc_gbs = pc_bytes / (pc_ms / 1e3) / 1e9
