@@ -243,6 +243,16 @@ ROUTE_CASES = [
     (300, 64, 40, 3, torch.float32, "softmax_topk", (1, 1, 0), 0.02, None, None),
     # 32 experts exactly: the one-kernel router at its widest
     (700, 1024, 32, 4, torch.bfloat16, "softmax_full", (1, 1, 0), None, 1.5, None),
+    # one-kernel router: W_r exactly at its 96 KiB shared-memory limit; 5
+    # experts padded to 8 zero rows with a ragged vector count (D = 520);
+    # 12 experts (16 rows) with the group limit
+    (150, 6144, 8, 2, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
+    (333, 520, 5, 2, torch.bfloat16, "softmax_full", (1, 1, 0), None, 1.0, None),
+    (200, 320, 12, 3, torch.bfloat16, "sigmoid_bias", (4, 2, 2), None, None, 0.1),
+    # few experts but W_r over that limit: the router GEMM (bf16 on tensor
+    # cores, fp32 on the FMA pipes), then the select kernel
+    (257, 8192, 8, 2, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
+    (130, 4096, 8, 2, torch.float32, "softmax_topk", (1, 1, 0), 0.02, None, None),
     # group scores over more than 8 keys (the warp-round path)
     (333, 128, 64, 6, torch.bfloat16, "sigmoid_bias", (4, 2, 12), None, None, 0.2),
     (300, 128, 96, 8, torch.bfloat16, "softmax_topk", (6, 3, 16), None, None, None),
