@@ -400,6 +400,10 @@ FFN_CASES = [
      torch.bfloat16),
     (7, 320, 128, [40, 170, 3, 81, 128 + 65, 0, 97], torch.bfloat16),
     (2, 768, 384, [1, 64], torch.bfloat16),
+    # more tiles than SMs in both projections (21 row blocks, D = 2048),
+    # with swapped tails, and fewer down tiles than SMs (16 row blocks)
+    (4, 2048, 128, [600, 700, 513, 640], torch.bfloat16),
+    (3, 2048, 128, [600, 700, 513], torch.bfloat16),
     # long down-projection contractions (32 and 16 K blocks) over few tiles,
     # swapped and normal
     (4, 512, 2048, [300, 40, 0, 129], torch.bfloat16),
