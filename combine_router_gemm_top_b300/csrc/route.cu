@@ -1,5 +1,6 @@
 // moe_route kernels: router GEMM (tcgen05 split-K for bf16, fp32 FMA for
-// fp32), then per-token scoring, group-limited top-k and gates
+// fp32), then per-token scoring, group-limited top-k and gates; for up to
+// 32 experts with a small W_r, both in one warp-per-token kernel
 // ("Expert Parallelism in LLMs", The Execution Pipeline, step 1 "Router
 // Gating and Softmax Selection": g_t = Softmax(TopK(W_g x_t, k))).
 #include <cuda.h>
