@@ -71,10 +71,14 @@ def capture_stages(stages, dev):
 K_graph_cap = 200
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from ncu, keyed by
-# (workload, T, step): the grouped FFN's one launch (up and down projection)
-# on the Mixtral-like layer, 3.0816 GB read + 145.4 MB written, taken on the
-# current kernel.
-NCU_DRAM_BYTES = {("mixtral_bf16", 2048, "ffn"): 3.2270e9}
+# (workload, T, E, step), for the grouped FFN's one launch (up and down
+# projection) of the current kernel:
+#   Mixtral-like   3.0816 GB read + 145.4 MB written
+#   DeepSeek-like 23.3931 GB read + 598.7 MB written
+#   Switch-like    522.6 MB read +  17.4 MB written
+NCU_DRAM_BYTES = {("mixtral_bf16", 2048, 8, "ffn"): 3.2270e9,
+                  ("deepseek_bf16", 4096, 256, "ffn"): 2.39918e10,
+                  ("switch_bf16", 16384, 64, "ffn"): 5.400e8}
 
 # tokens of the bounded CPU-oracle sample, per workload (about 10-30 s of
 # host work)
@@ -390,7 +394,7 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
     # DRAM bytes (read + write) of one launch of the dominant kernel, from an
     # ncu capture of the same kernel on the same workload; re-take it when
     # the kernel changes.
-    dram = NCU_DRAM_BYTES.get((wl.name, wl.T, dom))
+    dram = NCU_DRAM_BYTES.get((wl.name, wl.T, wl.E, dom))
     if dram is not None:
         roof["traffic"] = dram
         roof["traffic_over_algorithmic"] = round(
