@@ -83,3 +83,17 @@ def test_route_work_and_bound(bench):
     assert m["route"]["bound"] == "hbm"
     assert m["route"]["roofline_ms"] == pytest.approx(
         m["route"]["bytes"] / (PEAKS["hbm_gbs"] * 1e9) * 1e3)
+
+
+def test_traffic_keys_match_workload_shapes(bench):
+    # each ncu traffic figure is looked up by (workload, T, E, step); a key
+    # whose shape differs from the workload's would never be found
+    for (name, T, E, step), v in bench.NCU_DRAM_BYTES.items():
+        wl = W.WORKLOADS[name]
+        assert (wl.T, wl.E) == (T, E), name
+        assert step == "ffn" and not wl.identity_experts
+        # a figure of the right order against all experts' weights plus
+        # activations: above a quarter of them (the Switch-like layer has 20
+        # of 64 experts active) and below 1.2x
+        m = bench.kernel_models(wl, wl.T * wl.k, 2, PEAKS)
+        assert 0.25 * m["ffn"]["bytes"] < v < 1.2 * m["ffn"]["bytes"], name
