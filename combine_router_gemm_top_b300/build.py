@@ -5,6 +5,7 @@
 The library is the product's compute path: every kernel of the MoE layer
 lives in csrc/ and is reached through the C ABI of include/moe.h.
 """
+import glob
 import os
 import subprocess
 import sys
@@ -16,7 +17,6 @@ LIB = os.path.join(HERE, "libmoe.so")
 SOURCES = ["api.cu", "route.cu", "layout.cu", "permute_combine.cu",
            "grouped_ffn.cu", "layout_noalloc.cu", "router_stats.cu",
            "dispatch_extras.cu", "backward.cu"]
-HEADERS = ["common.cuh", "ptx.cuh", "umma_gemm.cuh", "internal.h"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -24,11 +24,18 @@ FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
          "-I" + os.path.join(ROOT, "include")]
 
 
+def headers():
+    """Every header under csrc/: a change to any of them rebuilds the
+    library (each translation unit may include any header)."""
+    return sorted(os.path.basename(p) for ext in ("*.cuh", "*.h")
+                  for p in glob.glob(os.path.join(CSRC, ext)))
+
+
 def _stale():
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
+    deps = [os.path.join(CSRC, f) for f in SOURCES + headers()]
     deps.append(os.path.join(ROOT, "include", "moe.h"))
     deps.append(os.path.abspath(__file__))
     return any(os.path.getmtime(d) > t for d in deps)

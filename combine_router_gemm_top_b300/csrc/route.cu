@@ -15,41 +15,18 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// fp32 sigmoid used for selection keys.  Selection is an integer decision
-// taken on fp32 values, so both this library and any checker must evaluate
-// the key with the same fp32 operations.  The recipe (Cody-Waite range
-// reduction, W. J. Cody and W. Waite, "Software Manual for the Elementary
-// Functions", 1980, followed by the degree-7 Taylor polynomial of exp on
-// |r| <= ln2/2 in Horner form), every step one IEEE round-to-nearest fp32
-// operation with no fused multiply-add:
-//   z  = clamp(-l, -87, 88)
-//   n  = rint(z * LOG2E)
-//   r  = (z - n*LN2_HI) - n*LN2_LO          (n*LN2_HI is exact)
-//   p  = c7; p = p*r + c_i for i = 6..0      (c_i = fp32(1/i!))
-//   e  = p * 2^n                             (exact: the result is normal)
-//   s  = 1 / (1 + e)
-// LN2_HI is ln 2 in fp32 with the low 12 mantissa bits cleared, LN2_LO the
-// fp32 rounding of the remainder.  Maximum error against the exact sigmoid
-// is a few fp32 ulp.
+// Sigmoid score of the sigmoid router: s = fp32(1 / (1 + e^-l)), evaluated in
+// float64 and rounded once to fp32 (round to nearest even).  The selection key
+// is then s + b_e, added in fp32.  A float64 evaluation carries a few float64
+// ulp of error, so s is the correctly rounded sigmoid except where the exact
+// value lies within that distance of the midpoint between two fp32 values.
+// For l >= 18 the exact sigmoid is above 1 - 2^-25 and rounds to 1.0, so no
+// exponential is evaluated there.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float sigmoid_key_f32(float l) {
-  const float kLog2e = 1.44269502162933349609375f;   // 0x3FB8AA3B
-  const float kLn2Hi = 0.693115234375f;              // 0x3F317000
-  const float kLn2Lo = 3.194618329871446e-05f;       // 0x3805FDF4
-  const float c[8] = {1.0f, 1.0f, 0.5f, 0.1666666716337204f,
-                      0.0416666679084301f, 0.008333333767950535f,
-                      0.0013888889225199819f, 0.00019841270113829523f};
-  float z = -l;
-  z = fminf(fmaxf(z, -87.0f), 88.0f);
-  const float n = rintf(__fmul_rn(z, kLog2e));
-  const float r = __fsub_rn(__fsub_rn(z, __fmul_rn(n, kLn2Hi)),
-                            __fmul_rn(n, kLn2Lo));
-  float p = c[7];
-#pragma unroll
-  for (int i = 6; i >= 0; --i) p = __fadd_rn(__fmul_rn(p, r), c[i]);
-  const float two_n = __int_as_float((static_cast<int>(n) + 127) << 23);
-  const float e = __fmul_rn(p, two_n);
-  return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
+__device__ __forceinline__ float sigmoid_score(float l) {
+  if (l >= 18.0f) return 1.0f;
+  const double e = exp(-static_cast<double>(l));
+  return __double2float_rn(1.0 / (1.0 + e));
 }
 
 // Order-preserving code of an fp32 selection key: for keys a, b (+0 and -0
@@ -119,7 +96,7 @@ __device__ __forceinline__ void select_token(const RouteSelectArgs& a,
       if (a.logits_out != nullptr) a.logits_out[t * E + e] = lg[i];
       float k = lg[i];
       if (a.score == MOE_SCORE_SIGMOID_BIAS) {
-        k = sigmoid_key_f32(k);
+        k = sigmoid_score(k);
         if (a.sel_bias != nullptr) k = __fadd_rn(k, a.sel_bias[e]);
       }
       key[i] = k;
@@ -242,7 +219,7 @@ __device__ __forceinline__ void select_token(const RouteSelectArgs& a,
     z = warp_sum(z);
     g = slot ? expf(my_logit - mx) / z : 0.0f;
   } else {
-    const float sg = slot ? sigmoid_key_f32(my_logit) : 0.0f;
+    const float sg = slot ? sigmoid_score(my_logit) : 0.0f;
     g = sg / warp_sum(sg);
   }
   if (slot) {
@@ -400,7 +377,7 @@ __global__ void route_gemm_f32_kernel(int T, int D, int E, const float* x,
 
 __global__ void sigmoid_key_kernel(const float* l, float* out, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) out[i] = sigmoid_key_f32(l[i]);
+  if (i < n) out[i] = sigmoid_score(l[i]);
 }
 
 moe_status launch_sigmoid_key(const float* l, float* out, int n,

@@ -510,10 +510,13 @@ MOE_API size_t moe_route_backward_workspace_size(const moe_route_cfg* cfg);
 MOE_API moe_status moe_selftest_bounded_wait(int32_t* status, uint64_t limit_ns,
                                      moe_stream_t stream);
 
-/* Test hook for the selection key of MOE_SCORE_SIGMOID_BIAS: out[i] = the
- * fp32 sigmoid moe_route evaluates for logit l[i] (n values, device
- * pointers).  Selection is an integer decision taken on these fp32 values,
- * so a checker must reproduce them bit for bit. */
+/* Test hook for the selection score of MOE_SCORE_SIGMOID_BIAS: out[i] =
+ * fp32(1 / (1 + exp(-l[i]))), the sigmoid evaluated in float64 and rounded
+ * once to fp32, exactly as moe_route ranks experts by it before adding the
+ * bias (n values, device pointers).  Selection is an integer decision taken
+ * on these fp32 values; a checker that evaluates the same definition in
+ * float64 agrees bit for bit except within a few float64 ulp of an fp32
+ * rounding midpoint. */
 MOE_API moe_status moe_selftest_sigmoid_key(const float* l, float* out,
                                             int32_t n, moe_stream_t stream);
 

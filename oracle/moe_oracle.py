@@ -22,10 +22,9 @@ per-rank send counts and displacements the dispatch exchange would take
 Readings taken where the pages leave a step open (each is also listed in the
 design notes):
   * selection key: the fp32 logit in softmax modes (softmax is monotone);
-    in sigmoid mode key = fp32(s + b_e) with s the fp32 sigmoid of
-    sigmoid_key_f32 below.  Selection is an integer decision taken on fp32
-    values, so the oracle takes it in the kernel's precision with the same
-    published fp32 recipe (pinned against the exact sigmoid);
+    in sigmoid mode key = fp32(s + b_e), where s = fp32(sigmoid(l)) is the
+    sigmoid evaluated in float64 and rounded once to fp32, and the bias is
+    added in fp32 (round to nearest even);
   * ties: equal keys go to the lower expert index, equal group scores to the
     lower group index; slot order is descending key;
   * group score: sum of the top `group_score_topk` biased keys of the group,
@@ -81,36 +80,10 @@ def sigmoid_f64(logits):
     return 1.0 / (1.0 + np.exp(-l))
 
 
-# fp32 constants of the selection-key sigmoid: 1/ln 2; ln 2 split into a
-# high part with the low 12 mantissa bits cleared (so n * LN2_HI is exact
-# for |n| < 2^7) and the fp32 rounding of the remainder; Taylor
-# coefficients 1/i! rounded to fp32.
-_LOG2E = F32(1.0 / math.log(2.0))
-_LN2_HI = np.array([F32(math.log(2.0)).view(np.uint32) & np.uint32(0xFFFFF000)],
-                   dtype=np.uint32).view(F32)[0]
-_LN2_LO = F32(math.log(2.0) - float(_LN2_HI))
-_TAYLOR = [F32(1.0 / math.factorial(i)) for i in range(8)]
-
-
-def sigmoid_key_f32(logits):
-    """fp32 sigmoid by Cody-Waite range reduction (W. J. Cody and
-    W. Waite, "Software Manual for the Elementary Functions", 1980) and the
-    degree-7 Taylor polynomial of exp, every step one IEEE fp32 operation
-    (numpy float32 arithmetic, no fused multiply-add):
-        z = clamp(-l, -87, 88);  n = rint(z * log2 e)
-        r = (z - n*LN2_HI) - n*LN2_LO;  p = Horner(r);  e = p * 2^n
-        s = 1 / (1 + e)
-    Its error against the exact sigmoid is a few fp32 ulp (pinned)."""
-    l = np.asarray(logits, dtype=F32)
-    z = np.minimum(np.maximum(-l, F32(-87.0)), F32(88.0)).astype(F32)
-    n = np.rint(z * _LOG2E).astype(F32)
-    r = ((z - n * _LN2_HI) - n * _LN2_LO).astype(F32)
-    p = np.full(z.shape, _TAYLOR[7], dtype=F32)
-    for c in reversed(_TAYLOR[:7]):
-        p = (p * r + c).astype(F32)
-    two_n = np.ldexp(np.ones(z.shape, dtype=F32), n.astype(np.int32))
-    e = (p * two_n.astype(F32)).astype(F32)
-    return (F32(1.0) / (F32(1.0) + e)).astype(F32)
+def sigmoid_f32(logits):
+    """fp32(sigmoid(l)): the float64 sigmoid rounded once to fp32.  This is
+    the score the sigmoid router ranks by before its bias is added."""
+    return sigmoid_f64(logits).astype(F32)
 
 
 def selection_keys(logits, mode, sel_bias=None):
@@ -127,7 +100,7 @@ def selection_keys(logits, mode, sel_bias=None):
     if mode in (SOFTMAX_TOPK, SOFTMAX_FULL):
         return logits.copy()
     if mode == SIGMOID_BIAS:
-        s = sigmoid_key_f32(logits)
+        s = sigmoid_f32(logits)
         b = np.zeros(logits.shape[-1], F32) if sel_bias is None else \
             np.asarray(sel_bias, dtype=F32)
         return (s + b).astype(F32)

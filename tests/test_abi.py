@@ -27,6 +27,17 @@ def declared_functions():
                                  text)))
 
 
+def test_every_csrc_file_is_built_or_watched():
+    # an edit to any file under csrc/ must rebuild the library
+    csrc = os.path.join(ROOT, "combine_router_gemm_top_b300", "csrc")
+    files = sorted(f for f in os.listdir(csrc)
+                   if os.path.isfile(os.path.join(csrc, f)))
+    assert files
+    watched = set(B.SOURCES) | set(B.headers())
+    assert [f for f in files if f not in watched] == []
+    assert "umma_ffn.cuh" in B.headers()
+
+
 def test_header_declares_the_five_calls():
     names = declared_functions()
     for n in ("moe_route", "moe_dispatch_layout", "moe_permute",

@@ -314,18 +314,32 @@ def test_route_group_ties_go_to_lower_index(groups):
 
 
 def test_sigmoid_key_bit_exact():
-    # the selection key is an integer decision's input: the device function
-    # and the oracle's fp32 recipe must agree bit for bit
+    # the selection score is an integer decision's input: the device's
+    # fp32(sigmoid(l)) must equal the oracle's float64 sigmoid rounded once
+    # (itself pinned against scipy's expit and a 50-digit evaluation).  A
+    # difference is allowed only where the float64 value sits within 2^-44
+    # (relative) of the midpoint between two fp32 values, where two float64
+    # evaluations may round either way; none is expected.
     l = np.concatenate([np.linspace(-95, 95, 1 << 20),
                         np.random.default_rng(8).standard_normal(1 << 18) * 6,
-                        [0.0, -0.0, 87.0, -87.0, 88.0, -88.0, 1e-30, -1e-30]]
-                       ).astype(np.float32)
+                        [0.0, -0.0, 17.9, 18.0, 87.0, -87.0, 88.0, -88.0,
+                         103.0, -103.0, 1e-30, -1e-30]]).astype(np.float32)
     dl = torch.tensor(l, device=DEV)
     out = torch.empty_like(dl)
     L.moe_selftest_sigmoid_key(dl, out)
     torch.cuda.synchronize()
-    ref = O.sigmoid_key_f32(l)
-    assert (out.cpu().numpy().view(np.uint32) == ref.view(np.uint32)).all()
+    got = out.cpu().numpy()
+    ref = O.sigmoid_f32(l)
+    diff = got.view(np.uint32) != ref.view(np.uint32)
+    if diff.any():
+        s64 = O.sigmoid_f64(l[diff])
+        lo = np.minimum(got[diff], ref[diff]).astype(np.float64)
+        hi = np.maximum(got[diff], ref[diff]).astype(np.float64)
+        adjacent = np.nextafter(lo.astype(np.float32), np.float32(2)) == \
+            hi.astype(np.float32)
+        near_mid = np.abs(s64 - (lo + hi) / 2) <= 2.0 ** -44 * s64
+        assert (adjacent & near_mid).all(), l[diff][~(adjacent & near_mid)][:8]
+    assert diff.sum() <= 2
 
 
 # ------------------------------------------------------------ permute/combine

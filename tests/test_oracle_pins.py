@@ -156,7 +156,8 @@ def test_group_limited_brute_force():
         idx, _ = O.route_from_logits(logits, k, O.SIGMOID_BIAS, bias,
                                      n_groups=G, topk_groups=TG,
                                      group_score_topk=gk)
-        keys = (O.sigmoid_key_f32(logits[0]) + bias).astype(np.float32)
+        s = scipy.special.expit(logits[0].astype(np.float64)).astype(np.float32)
+        keys = (s + bias).astype(np.float32)
         # group score: the best sum of any gk keys in the group, in fp32
         # (order-free for two terms)
         score = []
@@ -169,26 +170,50 @@ def test_group_limited_brute_force():
         assert idx[0].tolist() == _brute_topk(keys, k, eligible)
 
 
-def test_sigmoid_key_within_few_ulp_of_exact():
-    # dense grid over the whole clamp range plus random points
-    l = np.concatenate([np.linspace(-90, 90, 200001),
-                        np.random.default_rng(1).standard_normal(100000) * 4]
-                       ).astype(np.float32)
-    got = O.sigmoid_key_f32(l).astype(np.float64)
-    ref = scipy.special.expit(l.astype(np.float64))
-    ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
-    inside = np.abs(l) <= 87
-    assert (np.abs(got - ref)[inside] <= 4 * ulp[inside]).all()
-    # clamped tails stay within the clamp value's sigmoid
-    assert (got[l > 87] == 1.0).all()
-    assert (got[l < -88] <= scipy.special.expit(-88.0) * (1 + 1e-6)).all()
+def _sigmoid_grid():
+    # dense grid over [-95, 95] (past both ends of fp32's useful range),
+    # random points, and the special values
+    return np.concatenate([np.linspace(-95, 95, 400001),
+                           np.random.default_rng(1).standard_normal(200000) * 4,
+                           [0.0, -0.0, 1e-30, -1e-30, 87.0, -87.0, 88.0,
+                            -88.0, 103.0, -103.0]]).astype(np.float32)
+
+
+def test_sigmoid_key_is_expit_rounded_once():
+    # the selection score fp32(sigmoid(l)) against scipy's float64 expit
+    # rounded once, bit for bit, over the whole range
+    l = _sigmoid_grid()
+    got = O.sigmoid_f32(l)
+    ref = scipy.special.expit(l.astype(np.float64)).astype(np.float32)
+    assert got.dtype == np.float32
+    assert (got.view(np.uint32) == ref.view(np.uint32)).all()
+    # closed forms: sigmoid(0) = 1/2 exactly, saturation at the ends
+    assert O.sigmoid_f32(np.float32([0.0, -0.0])).tolist() == [0.5, 0.5]
+    assert O.sigmoid_f32(np.float32([95.0]))[0] == 1.0
+    assert 0.0 < O.sigmoid_f32(np.float32([-95.0]))[0] < 1e-41
     # monotone non-decreasing on the sorted grid
-    g = O.sigmoid_key_f32(np.sort(l))
+    g = O.sigmoid_f32(np.sort(l))
     assert (np.diff(g.astype(np.float64)) >= 0).all()
-    # the constants are the stated splits of ln 2
-    assert float(O._LN2_HI) + float(O._LN2_LO) == pytest.approx(
-        math.log(2.0), abs=1e-11)
-    assert int(np.float32(O._LN2_HI).view(np.uint32)) & 0xFFF == 0
+
+
+def test_sigmoid_key_correctly_rounded():
+    # 50-digit evaluation of 1/(1+e^-l) rounded to the nearest fp32 value:
+    # the oracle's score is the correctly rounded sigmoid on a sample
+    # spanning the range (a float64 evaluation can differ only within a
+    # few float64 ulp of an fp32 rounding boundary)
+    import mpmath
+    mpmath.mp.dps = 50
+    rng = np.random.default_rng(5)
+    l = np.concatenate([rng.uniform(-90, 90, 1500), rng.standard_normal(1500)]
+                       ).astype(np.float32)
+    got = O.sigmoid_f32(l)
+    for li, gi in zip(l.tolist(), got.tolist()):
+        exact = 1 / (1 + mpmath.exp(-mpmath.mpf(li)))
+        lo = np.float32(float(exact))
+        # the two fp32 neighbours around the exact value; the nearer wins
+        cands = [lo, np.nextafter(lo, np.float32(-1)), np.nextafter(lo, np.float32(2))]
+        best = min(cands, key=lambda c: abs(mpmath.mpf(float(c)) - exact))
+        assert gi == float(best), (li, gi, float(best))
 
 
 def test_sigmoid_bias_selects_but_does_not_weight():
