@@ -567,13 +567,14 @@ def run_extras(args, local_rank, workload):
             E, cap, D, layer.dcode, layer.expert_counts, xpad)),
             nbytes=(rows - n_kept) * D * es)
         put("padded_permute", timed(lambda: L.moe_permute(
-            T, k, D, layer.dcode, x, dst_p, xpad)),
+            T, k, D, layer.dcode, x, dst_p, xpad, layer.status)),
             nbytes=T * D * es + n_kept * D * es + P * 4)
         put("padded_ffn", timed(lambda: L.moe_grouped_ffn(
             E, D, wl.F, rows, layer.dcode, xpad, off_p, layer.w13, layer.w2,
             ypad, fws, st)), flops=6.0 * D * wl.F * rows)
         put("padded_combine", timed(lambda: L.moe_combine(
-            T, k, D, layer.dcode, ypad, dst_p, layer.topk_gate, y)),
+            T, k, D, layer.dcode, ypad, dst_p, layer.topk_gate, y,
+            layer.status)),
             nbytes=n_kept * D * es + T * D * es + P * 8)
     torch.cuda.synchronize()
     if st.item() != 0 or layer.device_status() != 0:
@@ -626,7 +627,7 @@ def run_train(args, local_rank, workload):
         rec(1)
         L.moe_combine_backward(wl.T, wl.k, wl.D, layer.dcode, dy, b["ya"],
                                b["dst_a"], layer.topk_gate, b["dga"],
-                               b["dgate"], stream)
+                               b["dgate"], layer.status, stream)
         L.moe_aligned_fill(wl.E, wl.D, layer.dcode, layer.expert_offsets,
                            b["off_a"], b["dga"], stream)
         rec(2)
@@ -636,7 +637,7 @@ def run_train(args, local_rank, workload):
                                    b["bwd_ws"], layer.status, stream)
         rec(3)
         L.moe_permute_backward(wl.T, wl.k, wl.D, layer.dcode, b["dxa"],
-                               b["dst_a"], b["dx"], stream)
+                               b["dst_a"], b["dx"], layer.status, stream)
         rec(4)
         L.moe_route_backward(layer.cfg, x, layer.w_r, layer.logits,
                              layer.topk_idx, b["dgate"], b["dlogits"],

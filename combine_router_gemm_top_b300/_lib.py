@@ -45,9 +45,9 @@ EXPORTED = ["moe_route_workspace_size", "moe_route_launches", "moe_route",
             "moe_aligned_fill", "moe_combine_backward",
             "moe_permute_backward", "moe_grouped_ffn_backward_workspace_size",
             "moe_grouped_ffn_backward", "moe_route_backward",
-            "moe_route_backward_workspace_size",
+            "moe_route_backward_workspace_size", "moe_expert_capacity",
             "moe_status_str", "moe_abi_version"]
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 
 class MoeError(RuntimeError):
@@ -82,11 +82,15 @@ _SIGS = {
     "moe_dispatch_layout_noalloc": (_i32, [_i32, _i32, _i32, _i32, _i32,
                                            _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                            _vp, _vp, _vp, _vp]),
-    "moe_permute": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "moe_permute": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _vp,
+                           _vp]),
     "moe_grouped_ffn_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "moe_grouped_ffn": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
                                _vp, _vp, _vp, _sz, _vp, _vp]),
-    "moe_combine": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "moe_combine": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32,
+                           _vp, _vp]),
+    "moe_expert_capacity": (_i32, [ctypes.c_int64, ctypes.c_int64, _i32, _i32,
+                                   _i32]),
     "moe_router_stats_workspace_size": (_sz, [_i32, _i32]),
     "moe_router_stats": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp,
                                 ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _sz,
@@ -102,9 +106,9 @@ _SIGS = {
                                   _vp, _vp, _vp, _vp]),
     "moe_aligned_fill": (_i32, [_i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "moe_combine_backward": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp,
-                                    _vp, _vp, _vp, _vp]),
+                                    _vp, _vp, _vp, _i32, _vp, _vp]),
     "moe_permute_backward": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp,
-                                    _vp]),
+                                    _i32, _vp, _vp]),
     "moe_grouped_ffn_backward_workspace_size": (_sz, [_i32, _i32, _i32, _i32,
                                                       _i32]),
     "moe_grouped_ffn_backward": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp,
@@ -236,8 +240,15 @@ def moe_dispatch_layout_noalloc(T, k, E, R, capacity, topk_idx,
         _p(status), _stream(stream)), "moe_dispatch_layout_noalloc")
 
 
-def moe_permute(T, k, D, dtype, x, dst_row, xp, stream=None):
+def _rows(buf, max_rows):
+    # rows of a [rows, D] buffer unless the caller names fewer
+    return int(buf.shape[0]) if max_rows is None else int(max_rows)
+
+
+def moe_permute(T, k, D, dtype, x, dst_row, xp, status=None, stream=None,
+                max_rows=None):
     _check(load().moe_permute(T, k, D, dtype, _p(x), _p(dst_row), _p(xp),
+                              _rows(xp, max_rows), _p(status),
                               _stream(stream)), "moe_permute")
 
 
@@ -254,10 +265,17 @@ def moe_grouped_ffn(E, D, F, max_rows, dtype, xp, expert_offsets, w13, w2,
                                   _stream(stream)), "moe_grouped_ffn")
 
 
-def moe_combine(T, k, D, dtype, yp, dst_row, topk_gate, y, stream=None):
+def moe_combine(T, k, D, dtype, yp, dst_row, topk_gate, y, status=None,
+                stream=None, max_rows=None):
     _check(load().moe_combine(T, k, D, dtype, _p(yp), _p(dst_row),
-                              _p(topk_gate), _p(y), _stream(stream)),
+                              _p(topk_gate), _p(y), _rows(yp, max_rows),
+                              _p(status), _stream(stream)),
            "moe_combine")
+
+
+def moe_expert_capacity(cf_num, cf_den, T, k, E) -> int:
+    """ceil(cf_num / cf_den * k * T / E); -1 for invalid arguments."""
+    return load().moe_expert_capacity(int(cf_num), int(cf_den), T, k, E)
 
 
 def moe_router_stats_workspace_size(T, E) -> int:
@@ -321,16 +339,21 @@ def moe_aligned_fill(E, D, dtype, expert_offsets, offsets_aligned, buf,
 
 
 def moe_combine_backward(T, k, D, dtype, dy, yp, dst_row, topk_gate, dyp,
-                         dgate, stream=None):
+                         dgate, status=None, stream=None, max_rows=None):
+    rows = _rows(yp, max_rows if max_rows is not None else
+                 min(int(yp.shape[0]), int(dyp.shape[0])))
     _check(load().moe_combine_backward(T, k, D, dtype, _p(dy), _p(yp),
                                        _p(dst_row), _p(topk_gate), _p(dyp),
-                                       _p(dgate), _stream(stream)),
+                                       _p(dgate), rows, _p(status),
+                                       _stream(stream)),
            "moe_combine_backward")
 
 
-def moe_permute_backward(T, k, D, dtype, dxp, dst_row, dx, stream=None):
+def moe_permute_backward(T, k, D, dtype, dxp, dst_row, dx, status=None,
+                         stream=None, max_rows=None):
     _check(load().moe_permute_backward(T, k, D, dtype, _p(dxp), _p(dst_row),
-                                       _p(dx), _stream(stream)),
+                                       _p(dx), _rows(dxp, max_rows),
+                                       _p(status), _stream(stream)),
            "moe_permute_backward")
 
 

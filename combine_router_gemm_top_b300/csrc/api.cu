@@ -188,25 +188,44 @@ static bool rows_ok(int32_t T, int32_t k, int32_t D, int32_t dtype) {
 
 moe_status moe_permute(int32_t T, int32_t k, int32_t D, int32_t dtype,
                        const void* x, const int32_t* dst_row, void* xp,
+                       int32_t max_rows, int32_t* status,
                        moe_stream_t stream) {
-  if (!rows_ok(T, k, D, dtype)) return MOE_ERR_INVALID;
+  if (!rows_ok(T, k, D, dtype) || max_rows < 0) return MOE_ERR_INVALID;
   if (T == 0) return MOE_OK;
-  if (x == nullptr || dst_row == nullptr || xp == nullptr) return MOE_ERR_INVALID;
+  if (x == nullptr || dst_row == nullptr || (xp == nullptr && max_rows > 0))
+    return MOE_ERR_INVALID;
   if (!aligned(x, 16) || !aligned(xp, 16)) return MOE_ERR_INVALID;
-  return launch_permute(T, k, D, dtype, x, dst_row, xp,
+  return launch_permute(T, k, D, dtype, x, dst_row, xp, max_rows, status,
                         reinterpret_cast<cudaStream_t>(stream), num_sms());
 }
 
 moe_status moe_combine(int32_t T, int32_t k, int32_t D, int32_t dtype,
                        const void* yp, const int32_t* dst_row,
-                       const float* topk_gate, void* y, moe_stream_t stream) {
-  if (!rows_ok(T, k, D, dtype)) return MOE_ERR_INVALID;
+                       const float* topk_gate, void* y, int32_t max_rows,
+                       int32_t* status, moe_stream_t stream) {
+  if (!rows_ok(T, k, D, dtype) || max_rows < 0) return MOE_ERR_INVALID;
   if (T == 0) return MOE_OK;
-  if (yp == nullptr || dst_row == nullptr || topk_gate == nullptr || y == nullptr)
+  if ((yp == nullptr && max_rows > 0) || dst_row == nullptr ||
+      topk_gate == nullptr || y == nullptr)
     return MOE_ERR_INVALID;
   if (!aligned(yp, 16) || !aligned(y, 16)) return MOE_ERR_INVALID;
-  return launch_combine(T, k, D, dtype, yp, dst_row, topk_gate, y,
-                        reinterpret_cast<cudaStream_t>(stream), num_sms());
+  return launch_combine(T, k, D, dtype, yp, dst_row, topk_gate, y, max_rows,
+                        status, reinterpret_cast<cudaStream_t>(stream),
+                        num_sms());
+}
+
+int32_t moe_expert_capacity(int64_t cf_num, int64_t cf_den, int32_t T,
+                            int32_t k, int32_t E) {
+  if (cf_num < 0 || cf_den <= 0 || T < 0 || k < 1 || E < 1) return -1;
+  // ceil(cf_num * k * T / (cf_den * E)); every product fits in 128 bits
+  const unsigned __int128 num = static_cast<unsigned __int128>(cf_num) *
+                                static_cast<uint64_t>(k) *
+                                static_cast<uint64_t>(T);
+  const unsigned __int128 den = static_cast<unsigned __int128>(cf_den) *
+                                static_cast<uint64_t>(E);
+  const unsigned __int128 c = (num + den - 1) / den;
+  if (c > static_cast<unsigned __int128>(INT32_MAX)) return -1;
+  return static_cast<int32_t>(c);
 }
 
 size_t moe_grouped_ffn_workspace_size(int32_t E, int32_t D, int32_t F,
@@ -371,30 +390,34 @@ moe_status moe_aligned_fill(int32_t E, int32_t D, int32_t dtype,
 moe_status moe_combine_backward(int32_t T, int32_t k, int32_t D, int32_t dtype,
                                 const void* dy, const void* yp,
                                 const int32_t* dst_row, const float* topk_gate,
-                                void* dyp, float* dgate, moe_stream_t stream) {
-  if (!rows_ok(T, k, D, dtype)) return MOE_ERR_INVALID;
+                                void* dyp, float* dgate, int32_t max_rows,
+                                int32_t* status, moe_stream_t stream) {
+  if (!rows_ok(T, k, D, dtype) || max_rows < 0) return MOE_ERR_INVALID;
   if (T == 0) return MOE_OK;
-  if (dy == nullptr || yp == nullptr || dst_row == nullptr ||
-      topk_gate == nullptr || dyp == nullptr || dgate == nullptr)
+  if (dy == nullptr || dst_row == nullptr || topk_gate == nullptr ||
+      dgate == nullptr ||
+      ((yp == nullptr || dyp == nullptr) && max_rows > 0))
     return MOE_ERR_INVALID;
   if (!aligned(dy, 16) || !aligned(yp, 16) || !aligned(dyp, 16))
     return MOE_ERR_INVALID;
   return launch_combine_backward(T, k, D, dtype, dy, yp, dst_row, topk_gate,
-                                 dyp, dgate,
+                                 dyp, dgate, max_rows, status,
                                  reinterpret_cast<cudaStream_t>(stream),
                                  num_sms());
 }
 
 moe_status moe_permute_backward(int32_t T, int32_t k, int32_t D, int32_t dtype,
                                 const void* dxp, const int32_t* dst_row,
-                                void* dx, moe_stream_t stream) {
-  if (!rows_ok(T, k, D, dtype)) return MOE_ERR_INVALID;
+                                void* dx, int32_t max_rows, int32_t* status,
+                                moe_stream_t stream) {
+  if (!rows_ok(T, k, D, dtype) || max_rows < 0) return MOE_ERR_INVALID;
   if (T == 0) return MOE_OK;
-  if (dxp == nullptr || dst_row == nullptr || dx == nullptr)
+  if ((dxp == nullptr && max_rows > 0) || dst_row == nullptr || dx == nullptr)
     return MOE_ERR_INVALID;
   if (!aligned(dxp, 16) || !aligned(dx, 16)) return MOE_ERR_INVALID;
-  return launch_combine(T, k, D, dtype, dxp, dst_row, nullptr, dx,
-                        reinterpret_cast<cudaStream_t>(stream), num_sms());
+  return launch_combine(T, k, D, dtype, dxp, dst_row, nullptr, dx, max_rows,
+                        status, reinterpret_cast<cudaStream_t>(stream),
+                        num_sms());
 }
 
 size_t moe_grouped_ffn_backward_workspace_size(int32_t E, int32_t D, int32_t F,

@@ -44,13 +44,15 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
                             const int32_t* __restrict__ dst_row,
                             const float* __restrict__ gate,
                             uint4* __restrict__ dyp,
-                            float* __restrict__ dgate) {
+                            float* __restrict__ dgate, int max_rows,
+                            int32_t* status) {
   constexpr int N = Vec16<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kBwdWarps + (threadIdx.x >> 5);
   const int64_t nw = static_cast<int64_t>(gridDim.x) * kBwdWarps;
   for (int64_t t = w0; t < n_tok; t += nw) {
-    const int32_t my_dst = lane < k ? __ldg(dst_row + t * k + lane) : -1;
+    const int32_t my_dst = checked_row(
+        lane < k ? __ldg(dst_row + t * k + lane) : -1, max_rows, status);
     const float my_g = lane < k ? __ldg(gate + t * k + lane) : 0.0f;
     const uint4* src = dy + t * nvec;
     float my_dot = 0.0f;
@@ -82,8 +84,9 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
 moe_status launch_combine_backward(int T, int k, int D, int dtype,
                                    const void* dy, const void* yp,
                                    const int32_t* dst_row, const float* gate,
-                                   void* dyp, float* dgate,
-                                   cudaStream_t stream, int num_sms) {
+                                   void* dyp, float* dgate, int max_rows,
+                                   int32_t* status, cudaStream_t stream,
+                                   int num_sms) {
   if (T == 0) return MOE_OK;
   const int nvec = static_cast<int>(D * dtype_bytes(dtype) / 16);
   const int64_t want = ceil_div(T, kBwdWarps);
@@ -93,12 +96,12 @@ moe_status launch_combine_backward(int T, int k, int D, int dtype,
     combine_backward_kernel<__nv_bfloat16><<<grid, kBwdWarps * 32, 0, stream>>>(
         T, k, nvec, static_cast<const uint4*>(dy),
         static_cast<const uint4*>(yp), dst_row, gate,
-        static_cast<uint4*>(dyp), dgate);
+        static_cast<uint4*>(dyp), dgate, max_rows, status);
   else
     combine_backward_kernel<float><<<grid, kBwdWarps * 32, 0, stream>>>(
         T, k, nvec, static_cast<const uint4*>(dy),
         static_cast<const uint4*>(yp), dst_row, gate,
-        static_cast<uint4*>(dyp), dgate);
+        static_cast<uint4*>(dyp), dgate, max_rows, status);
   return launch_status();
 }
 

@@ -19,6 +19,17 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// A caller-supplied buffer row id: ids at or past max_rows become -1 (the
+// pair is skipped, never read or written) and raise MOE_ERR_INDEX.
+__device__ __forceinline__ int32_t checked_row(int32_t r, int32_t max_rows,
+                                               int32_t* status) {
+  if (r >= max_rows) {
+    set_status(status, MOE_ERR_INDEX);
+    return -1;
+  }
+  return r;
+}
+
 __host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) {
   return (a + b - 1) / b;
 }

@@ -62,11 +62,12 @@ moe_status launch_layout(int T, int k, int E, int R, int capacity,
                          cudaStream_t stream);
 
 moe_status launch_permute(int T, int k, int D, int dtype, const void* x,
-                          const int32_t* dst_row, void* xp,
-                          cudaStream_t stream, int num_sms);
+                          const int32_t* dst_row, void* xp, int max_rows,
+                          int32_t* status, cudaStream_t stream, int num_sms);
 moe_status launch_combine(int T, int k, int D, int dtype, const void* yp,
                           const int32_t* dst_row, const float* gate, void* y,
-                          cudaStream_t stream, int num_sms);
+                          int max_rows, int32_t* status, cudaStream_t stream,
+                          int num_sms);
 
 size_t ffn_ws_bytes(int E, int D, int F, int max_rows, int dtype);
 moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
@@ -116,8 +117,9 @@ moe_status launch_grouped_ffn_backward(int E, int D, int F, int max_rows,
 moe_status launch_combine_backward(int T, int k, int D, int dtype,
                                    const void* dy, const void* yp,
                                    const int32_t* dst_row, const float* gate,
-                                   void* dyp, float* dgate,
-                                   cudaStream_t stream, int num_sms);
+                                   void* dyp, float* dgate, int max_rows,
+                                   int32_t* status, cudaStream_t stream,
+                                   int num_sms);
 moe_status launch_aligned_layout(int T, int k, int E, int align,
                                  const int32_t* topk_idx,
                                  const int32_t* dst_row,

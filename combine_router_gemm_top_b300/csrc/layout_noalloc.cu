@@ -13,13 +13,20 @@
 //    MOE_NOALLOC_LAYOUT_SCRATCH_BYTES (1 MiB); larger requests return
 //    MOE_ERR_UNSUPPORTED and launch nothing.
 //  - Set-up: the first call on each device, with that device current, looks
-//    up the array's device address (cudaGetSymbolAddress) and caches it.
-//    Make that first call before any stream capture.
+//    up the array's device address (cudaGetSymbolAddress) and caches it,
+//    keyed by the unique id of the device's current CUDA context.  If that
+//    context is destroyed and another created (cudaDeviceReset, or a host
+//    engine that resets the device), the module is loaded again and the
+//    array may move: the next call sees a new context id and looks the
+//    address up again.  Make the first call in each context before any
+//    stream capture.
 //  - Sharing: every call uses the same array and leaves the last call's
 //    histograms in it.  Nothing needs clearing: each call writes every cell
 //    it later reads.  Calls whose kernels overlap on the GPU (different
 //    streams with no ordering between them) race on the array.
 //  - No cudaMalloc, cudaFree or other allocating routine is called.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -32,24 +39,73 @@ static __device__ __align__(256) int32_t
     g_layout_scratch[MOE_NOALLOC_LAYOUT_SCRATCH_BYTES / sizeof(int32_t)];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
+struct ScratchSlot {
+  void* ptr;
+  unsigned long long ctx_id;   // context the address belongs to
+};
+ScratchSlot g_scratch[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
-// Device address of the array on the current device (nullptr on failure).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (cuCtxGetId, never
+// reused within a process); false when there is none or the driver lacks
+// the call.
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return static_cast<CtxGetCurrentFn>(nullptr);
+    }
+    return reinterpret_cast<CtxGetCurrentFn>(fn);
+  }();
+  static CtxGetIdFn get_id = [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return static_cast<CtxGetIdFn>(nullptr);
+    }
+    return reinterpret_cast<CtxGetIdFn>(fn);
+  }();
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the array in the current context (nullptr on failure).
 void* scratch_address() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return nullptr;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_layout_scratch) != cudaSuccess) {
-      cudaGetLastError();   // leave no pending error behind for the caller
-      return nullptr;
-    }
-    g_scratch_ptr[dev] = p;
+  unsigned long long id = 0;
+  if (g_scratch[dev].ptr != nullptr && current_context_id(&id) &&
+      id == g_scratch[dev].ctx_id)
+    return g_scratch[dev].ptr;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_layout_scratch) != cudaSuccess) {
+    cudaGetLastError();   // leave no pending error behind for the caller
+    g_scratch[dev].ptr = nullptr;
+    return nullptr;
   }
-  return g_scratch_ptr[dev];
+  // the lookup made the device's primary context current if it was not;
+  // without a context id the address is looked up again on every call
+  if (current_context_id(&id)) {
+    g_scratch[dev].ptr = p;
+    g_scratch[dev].ctx_id = id;
+  } else {
+    g_scratch[dev].ptr = nullptr;
+  }
+  return p;
 }
 
 }  // namespace

@@ -12,7 +12,9 @@
 //           traffic N*D*s read + T*D*s written.
 //
 // One warp per (token, row segment); each lane moves 16-byte vectors, up
-// to 4 in flight per step for memory-level parallelism.  A row is one
+// to 4 in flight per step for memory-level parallelism.  Row ids at or past
+// the buffer's max_rows are skipped (never read or written) and reported as
+// MOE_ERR_INDEX.  A row is one
 // segment unless there are too few tokens to keep HBM busy: then it is cut
 // into up to 4 segments of at least 128 vectors, each its own warp (for
 // combine only with k <= 4).
@@ -28,7 +30,8 @@ template <typename T>
 __global__ void __launch_bounds__(kRowWarps * 32)
     permute_kernel(int64_t n_tok, int k, int nvec, int nseg,
                    const uint4* __restrict__ x,
-                   const int32_t* __restrict__ dst_row, uint4* __restrict__ xp) {
+                   const int32_t* __restrict__ dst_row, uint4* __restrict__ xp,
+                   int max_rows, int32_t* status) {
   const int lane = threadIdx.x & 31;
   const int64_t warp_g = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kRowWarps;
@@ -38,7 +41,8 @@ __global__ void __launch_bounds__(kRowWarps * 32)
     const int v_begin = static_cast<int>(u - t * nseg) * segv;
     const int v_end = v_begin + segv;
     // lane j < k holds the destination row of slot j
-    const int32_t my_dst = lane < k ? __ldg(dst_row + t * k + lane) : -1;
+    const int32_t my_dst = checked_row(
+        lane < k ? __ldg(dst_row + t * k + lane) : -1, max_rows, status);
     const uint4* src = x + t * nvec;
     for (int v0 = v_begin + lane; v0 < v_end; v0 += 32 * kUnroll) {
       uint4 buf[kUnroll];
@@ -68,7 +72,8 @@ __global__ void __launch_bounds__(kRowWarps * 32)
     combine_kernel(int64_t n_tok, int k, int nvec, int nseg_arg,
                    const uint4* __restrict__ yp,
                    const int32_t* __restrict__ dst_row,
-                   const float* __restrict__ gate, uint4* __restrict__ y) {
+                   const float* __restrict__ gate, uint4* __restrict__ y,
+                   int max_rows, int32_t* status) {
   constexpr int N = Vec16<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t warp_g = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
@@ -79,7 +84,8 @@ __global__ void __launch_bounds__(kRowWarps * 32)
     const int64_t t = u / nseg;
     const int v_begin = static_cast<int>(u - t * nseg) * segv;
     const int v_end = v_begin + segv;
-    const int32_t my_dst = lane < k ? __ldg(dst_row + t * k + lane) : -1;
+    const int32_t my_dst = checked_row(
+        lane < k ? __ldg(dst_row + t * k + lane) : -1, max_rows, status);
     // gate == nullptr: unit gates (the permute backward sums the rows)
     const float my_g =
         lane < k ? (gate != nullptr ? __ldg(gate + t * k + lane) : 1.0f)
@@ -138,8 +144,8 @@ static unsigned row_grid(int64_t units, int num_sms) {
 }
 
 moe_status launch_permute(int T, int k, int D, int dtype, const void* x,
-                          const int32_t* dst_row, void* xp,
-                          cudaStream_t stream, int num_sms) {
+                          const int32_t* dst_row, void* xp, int max_rows,
+                          int32_t* status, cudaStream_t stream, int num_sms) {
   if (T == 0) return MOE_OK;
   const int nvec = static_cast<int>(D * dtype_bytes(dtype) / 16);
   const int nseg = row_segments(T, nvec, num_sms);
@@ -147,17 +153,18 @@ moe_status launch_permute(int T, int k, int D, int dtype, const void* x,
   if (dtype == MOE_BF16)
     permute_kernel<__nv_bfloat16><<<grid, kRowWarps * 32, 0, stream>>>(
         T, k, nvec, nseg, static_cast<const uint4*>(x), dst_row,
-        static_cast<uint4*>(xp));
+        static_cast<uint4*>(xp), max_rows, status);
   else
     permute_kernel<float><<<grid, kRowWarps * 32, 0, stream>>>(
         T, k, nvec, nseg, static_cast<const uint4*>(x), dst_row,
-        static_cast<uint4*>(xp));
+        static_cast<uint4*>(xp), max_rows, status);
   return launch_status();
 }
 
 moe_status launch_combine(int T, int k, int D, int dtype, const void* yp,
                           const int32_t* dst_row, const float* gate, void* y,
-                          cudaStream_t stream, int num_sms) {
+                          int max_rows, int32_t* status, cudaStream_t stream,
+                          int num_sms) {
   if (T == 0) return MOE_OK;
   const int nvec = static_cast<int>(D * dtype_bytes(dtype) / 16);
   // with more than 4 slots a token's gather already has enough independent
@@ -169,17 +176,17 @@ moe_status launch_combine(int T, int k, int D, int dtype, const void* yp,
   if (dtype == MOE_BF16) {
     if (nseg > 1)
       combine_kernel<__nv_bfloat16, true><<<grid, kRowWarps * 32, 0, stream>>>(
-          T, k, nvec, nseg, src, dst_row, gate, dst);
+          T, k, nvec, nseg, src, dst_row, gate, dst, max_rows, status);
     else
       combine_kernel<__nv_bfloat16, false><<<grid, kRowWarps * 32, 0, stream>>>(
-          T, k, nvec, 1, src, dst_row, gate, dst);
+          T, k, nvec, 1, src, dst_row, gate, dst, max_rows, status);
   } else {
     if (nseg > 1)
       combine_kernel<float, true><<<grid, kRowWarps * 32, 0, stream>>>(
-          T, k, nvec, nseg, src, dst_row, gate, dst);
+          T, k, nvec, nseg, src, dst_row, gate, dst, max_rows, status);
     else
       combine_kernel<float, false><<<grid, kRowWarps * 32, 0, stream>>>(
-          T, k, nvec, 1, src, dst_row, gate, dst);
+          T, k, nvec, 1, src, dst_row, gate, dst, max_rows, status);
   }
   return launch_status();
 }

@@ -19,7 +19,6 @@ counts stay on the device.
 """
 from __future__ import annotations
 
-import math
 from fractions import Fraction
 from typing import Optional
 
@@ -29,12 +28,18 @@ from . import _lib as L
 
 
 def expert_capacity(capacity_factor, T, k, E) -> int:
-    """C_expert = ceil(CF * k * T / E) in exact rational arithmetic; 0 means
-    dropless ("Expert Parallelism in LLMs", Static Capacity Factors and Token
-    Dropping)."""
+    """C_expert = ceil(CF * k * T / E) from the library's exact integer
+    evaluation (moe_expert_capacity), with CF passed as the exact ratio of
+    its decimal form; 0 means dropless ("Expert Parallelism in LLMs", Static
+    Capacity Factors and Token Dropping)."""
     if capacity_factor is None:
         return 0
-    return math.ceil(Fraction(str(capacity_factor)) * k * T / E)
+    cf = Fraction(str(capacity_factor))
+    c = L.moe_expert_capacity(cf.numerator, cf.denominator, T, k, E)
+    if c < 0:
+        raise ValueError(f"capacity factor {capacity_factor} for T={T} "
+                         f"k={k} E={E} is out of range")
+    return c
 
 
 class MoELayer:
@@ -129,7 +134,7 @@ class MoELayer:
 
     def permute(self, x, stream=None):
         L.moe_permute(self.T, self.k, self.D, self.dcode, x, self.dst_row,
-                      self.xp, stream)
+                      self.xp, self.status, stream)
 
     def grouped_ffn(self, stream=None):
         if self.identity:
@@ -142,7 +147,7 @@ class MoELayer:
         gate = self.topk_gate if topk_gate is None else topk_gate
         out = self.y if y is None else y
         L.moe_combine(self.T, self.k, self.D, self.dcode, self.yp,
-                      self.dst_row, gate, out, stream)
+                      self.dst_row, gate, out, self.status, stream)
         return out
 
     # ---------------------------------------------------------- padded
@@ -166,7 +171,7 @@ class MoELayer:
         self.dispatch_layout(topk_idx, stream)
         self.padded_layout(topk_idx, stream)
         L.moe_permute(self.T, self.k, self.D, self.dcode, x,
-                      self.dst_row_padded, self.xpad, stream)
+                      self.dst_row_padded, self.xpad, self.status, stream)
         if not self.identity:
             L.moe_grouped_ffn(self.E, self.D, self.F,
                               self.E * self.capacity, self.dcode, self.xpad,
@@ -176,7 +181,7 @@ class MoELayer:
         gate = self.topk_gate if topk_gate is None else topk_gate
         out = self.y if y is None else y
         L.moe_combine(self.T, self.k, self.D, self.dcode, self.ypad,
-                      self.dst_row_padded, gate, out, stream)
+                      self.dst_row_padded, gate, out, self.status, stream)
         return out
 
     # ---------------------------------------------------------- training
@@ -234,13 +239,13 @@ class MoELayer:
         L.moe_aligned_fill(E, D, self.dcode, self.expert_offsets, b["off_a"],
                            b["xa"], stream)
         L.moe_permute(self.T, self.k, D, self.dcode, x, b["dst_a"], b["xa"],
-                      stream)
+                      self.status, stream)
         if not self.identity:
             L.moe_grouped_ffn(E, D, self.F, b["rows"], self.dcode, b["xa"],
                               b["off_a"], self.w13, self.w2, b["ya"],
                               b["ffn_ws"], self.status, stream)
         L.moe_combine(self.T, self.k, D, self.dcode, b["ya"], b["dst_a"],
-                      self.topk_gate, self.y, stream)
+                      self.topk_gate, self.y, self.status, stream)
         self._x = x
         return self.y
 
@@ -252,7 +257,7 @@ class MoELayer:
         E, D = self.E, self.D
         L.moe_combine_backward(self.T, self.k, D, self.dcode, dy, b["ya"],
                                b["dst_a"], self.topk_gate, b["dga"],
-                               b["dgate"], stream)
+                               b["dgate"], self.status, stream)
         L.moe_aligned_fill(E, D, self.dcode, self.expert_offsets, b["off_a"],
                            b["dga"], stream)
         dxa = b["dga"]
@@ -264,7 +269,7 @@ class MoELayer:
                                        self.status, stream)
             dxa = b["dxa"]
         L.moe_permute_backward(self.T, self.k, D, self.dcode, dxa,
-                               b["dst_a"], b["dx"], stream)
+                               b["dst_a"], b["dx"], self.status, stream)
         L.moe_route_backward(self.cfg, self._x, self.w_r, self.logits,
                              self.topk_idx, b["dgate"], b["dlogits"],
                              b["dw_r"], b["dx"], b["route_bwd_ws"],

@@ -69,7 +69,8 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = 2, /* valid request outside what this build runs    */
   MOE_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed          */
   MOE_ERR_TIMEOUT = 4,     /* device: a bounded wait expired                */
-  MOE_ERR_INDEX = 5        /* device: an expert id outside [0, E)           */
+  MOE_ERR_INDEX = 5        /* device: an expert id outside [0, E), or a
+                              buffer row id outside the buffer            */
 } moe_status;
 
 typedef enum { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
@@ -200,7 +201,10 @@ MOE_API moe_status moe_dispatch_layout(int32_t T, int32_t k, int32_t E, int32_t 
  *  - Requires ceil(T*k / 2048) * E * 4 <= MOE_NOALLOC_LAYOUT_SCRATCH_BYTES,
  *    else returns MOE_ERR_UNSUPPORTED without launching.
  *  - The first call on each device (with that device current) looks up the
- *    array's device address; make it before any stream capture.  A failed
+ *    array's device address and caches it for that device's current CUDA
+ *    context; make it before any stream capture.  After the context is
+ *    destroyed and re-created (cudaDeviceReset) the next call looks the
+ *    address up again, so make that call before any capture too.  A failed
  *    lookup returns MOE_ERR_CUDA.
  *  - All calls share the array; overlapping calls on the GPU (unordered
  *    streams) race.  No cudaMalloc, cudaFree or other allocating call. */
@@ -215,11 +219,18 @@ MOE_API moe_status moe_dispatch_layout_noalloc(
 /* moe_permute -- xp[dst_row[t*k + j]] = x[t] for every kept pair
  * ("Expert Parallelism in LLMs", The Execution Pipeline, step 2: tokens
  * physically reordered into contiguous per-destination buffers).  Each
- * token row is read once and written to each of its kept destinations.
- *   x    [T, D] dtype in;  xp [>= n_kept, D] dtype out (rows not named by
- *        dst_row are left unwritten).  16-byte aligned. */
+ * token row is read once and written to each of its kept destinations
+ * (a scatter by dst_row, so x is read once rather than once per pair).
+ *   x         [T, D] dtype in, 16-byte aligned
+ *   dst_row   [T*k] int32 in (moe_dispatch_layout's): < 0 = dropped
+ *   xp        [max_rows, D] dtype out, 16-byte aligned; rows not named by
+ *             dst_row are left unwritten
+ *   max_rows  rows of xp.  A row id >= max_rows is never written: the pair
+ *             is skipped and MOE_ERR_INDEX is raised in `status` (nullable).
+ */
 MOE_API moe_status moe_permute(int32_t T, int32_t k, int32_t D, int32_t dtype,
                        const void* x, const int32_t* dst_row, void* xp,
+                       int32_t max_rows, int32_t* status,
                        moe_stream_t stream);
 
 /* Bytes of scratch moe_grouped_ffn needs: the SwiGLU hidden activations
@@ -260,10 +271,26 @@ MOE_API moe_status moe_grouped_ffn(int32_t E, int32_t D, int32_t F, int32_t max_
  * Pipeline, step 6 "Unpermutation and Weighted Reduction"; dropped pairs
  * contribute nothing, "Static Capacity Factors and Token Dropping").  The
  * residual connection is not added.  A token with no kept pair gets zeros.
- *   yp [>= n_kept, D] dtype; y [T, D] dtype out; 16-byte aligned. */
+ *   yp        [max_rows, D] dtype, 16-byte aligned
+ *   dst_row   [T*k] int32 in: < 0 = dropped
+ *   topk_gate [T, k] fp32 in
+ *   y         [T, D] dtype out, 16-byte aligned
+ *   max_rows  rows of yp.  A row id >= max_rows is never read: the pair
+ *             contributes nothing and MOE_ERR_INDEX is raised in `status`
+ *             (nullable). */
 MOE_API moe_status moe_combine(int32_t T, int32_t k, int32_t D, int32_t dtype,
                        const void* yp, const int32_t* dst_row,
-                       const float* topk_gate, void* y, moe_stream_t stream);
+                       const float* topk_gate, void* y, int32_t max_rows,
+                       int32_t* status, moe_stream_t stream);
+
+/* moe_expert_capacity -- C_expert = ceil(CF * k * T / E) with the capacity
+ * factor given as the exact ratio CF = cf_num / cf_den (1.25 = 5 / 4)
+ * ("Expert Parallelism in LLMs", Static Capacity Factors and Token
+ * Dropping), evaluated in exact integer arithmetic.  Returns the capacity
+ * to pass to moe_dispatch_layout, or -1 for cf_num < 0, cf_den <= 0, T < 0,
+ * k < 1, E < 1 or a result above INT32_MAX.  Host only. */
+MOE_API int32_t moe_expert_capacity(int64_t cf_num, int64_t cf_den, int32_t T,
+                                    int32_t k, int32_t E);
 
 /* ------------------------------------------------------------------------
  * Router statistics and load balancing
@@ -423,20 +450,26 @@ MOE_API moe_status moe_aligned_fill(int32_t E, int32_t D, int32_t dtype,
  *     dgate[t, j]     = dy[t] . yp[r]                (fp32 accumulation)
  * and dgate = 0 for a dropped pair.  Rows of dyp not named by dst_row are
  * left unwritten (moe_aligned_fill zeroes an aligned buffer's padding).
- *   dy [T, D], yp [rows, D], dyp [rows, D] dtype; dgate [T, k] fp32 out */
+ *   dy [T, D] dtype; yp, dyp [max_rows, D] dtype; dgate [T, k] fp32 out.
+ * A row id >= max_rows is neither read nor written: its dgate is 0 and
+ * MOE_ERR_INDEX is raised in `status` (nullable). */
 MOE_API moe_status moe_combine_backward(int32_t T, int32_t k, int32_t D,
                                         int32_t dtype, const void* dy,
                                         const void* yp, const int32_t* dst_row,
                                         const float* topk_gate, void* dyp,
-                                        float* dgate, moe_stream_t stream);
+                                        float* dgate, int32_t max_rows,
+                                        int32_t* status, moe_stream_t stream);
 
 /* moe_permute_backward -- backward of moe_permute:
  *     dx[t] = sum over kept slots j of dxp[dst_row[t*k + j]]
  * (fp32 accumulation in slot order, rounded once to dtype; zeros for a
- * token with no kept pair).  dxp [rows, D], dx [T, D] dtype. */
+ * token with no kept pair).  dxp [max_rows, D], dx [T, D] dtype.  A row id
+ * >= max_rows is never read and raises MOE_ERR_INDEX in `status`
+ * (nullable). */
 MOE_API moe_status moe_permute_backward(int32_t T, int32_t k, int32_t D,
                                         int32_t dtype, const void* dxp,
                                         const int32_t* dst_row, void* dx,
+                                        int32_t max_rows, int32_t* status,
                                         moe_stream_t stream);
 
 /* Bytes of scratch moe_grouped_ffn_backward needs: dH [max_rows, F],
@@ -526,7 +559,7 @@ MOE_API const char* moe_status_str(int32_t status);
 /* ABI version of this header (incremented on any signature change). */
 MOE_API int32_t moe_abi_version(void);
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

@@ -134,19 +134,50 @@ def test_layout_launches(lib):
 
 
 def test_permute_combine_reject(lib):
-    assert lib.moe_permute(10, 2, 12, L.MOE_BF16, FAKE, FAKE, FAKE, None) == \
-        L.MOE_ERR_INVALID                              # 24-byte rows
-    assert lib.moe_permute(10, 2, 16, L.MOE_BF16, None, FAKE, FAKE, None) == \
-        L.MOE_ERR_INVALID
-    assert lib.moe_permute(10, 2, 16, L.MOE_BF16, FAKE + 8, FAKE, FAKE,
+    R = 20   # rows of the expert-contiguous buffer
+    assert lib.moe_permute(10, 2, 12, L.MOE_BF16, FAKE, FAKE, FAKE, R, None,
+                           None) == L.MOE_ERR_INVALID   # 24-byte rows
+    assert lib.moe_permute(10, 2, 16, L.MOE_BF16, None, FAKE, FAKE, R, None,
                            None) == L.MOE_ERR_INVALID
-    assert lib.moe_combine(10, 40, 16, L.MOE_BF16, FAKE, FAKE, FAKE, FAKE,
-                           None) == L.MOE_ERR_INVALID   # k > 32
-    assert lib.moe_combine(10, 2, 16, 3, FAKE, FAKE, FAKE, FAKE, None) == \
+    assert lib.moe_permute(10, 2, 16, L.MOE_BF16, FAKE + 8, FAKE, FAKE, R,
+                           None, None) == L.MOE_ERR_INVALID
+    assert lib.moe_permute(10, 2, 16, L.MOE_BF16, FAKE, FAKE, FAKE, -1,
+                           None, None) == L.MOE_ERR_INVALID   # max_rows < 0
+    assert lib.moe_combine(10, 40, 16, L.MOE_BF16, FAKE, FAKE, FAKE, FAKE, R,
+                           None, None) == L.MOE_ERR_INVALID   # k > 32
+    assert lib.moe_combine(10, 2, 16, 3, FAKE, FAKE, FAKE, FAKE, R, None,
+                           None) == L.MOE_ERR_INVALID
+    assert lib.moe_combine(10, 2, 16, L.MOE_BF16, FAKE, FAKE, FAKE, FAKE, -5,
+                           None, None) == L.MOE_ERR_INVALID
+    assert lib.moe_combine_backward(10, 2, 16, L.MOE_BF16, FAKE, FAKE, FAKE,
+                                    FAKE, FAKE, FAKE, -1, None, None) == \
         L.MOE_ERR_INVALID
+    assert lib.moe_permute_backward(10, 2, 16, L.MOE_BF16, FAKE, FAKE, FAKE,
+                                    -1, None, None) == L.MOE_ERR_INVALID
     # nothing to do is not an error
-    assert lib.moe_permute(0, 2, 16, L.MOE_BF16, None, None, None, None) == \
-        L.MOE_OK
+    assert lib.moe_permute(0, 2, 16, L.MOE_BF16, None, None, None, 0, None,
+                           None) == L.MOE_OK
+
+
+def test_expert_capacity_matches_the_oracle(lib):
+    # the library's integer evaluation of ceil(CF * k * T / E) against the
+    # oracle's rational one over a grid of factors and shapes
+    import oracle.moe_oracle as O
+    from fractions import Fraction
+    for cf in ("0.5", "1", "1.0", "1.1", "1.25", "1.5", "2", "3.75", "0.01"):
+        f = Fraction(cf)
+        for T, k, E in [(256, 2, 8), (16384, 1, 64), (100, 2, 8), (10, 1, 4),
+                        (1, 1, 256), (0, 2, 8), (65536, 8, 128), (7, 3, 5)]:
+            got = lib.moe_expert_capacity(f.numerator, f.denominator, T, k, E)
+            assert got == O.expert_capacity(cf, T, k, E), (cf, T, k, E)
+    assert lib.moe_expert_capacity(5, 4, 256, 2, 8) == 80
+    assert lib.moe_expert_capacity(1, 1, 16384, 1, 64) == 256
+    assert lib.moe_expert_capacity(-1, 1, 10, 1, 4) == -1
+    assert lib.moe_expert_capacity(1, 0, 10, 1, 4) == -1
+    assert lib.moe_expert_capacity(1, 1, 10, 0, 4) == -1
+    assert lib.moe_expert_capacity(1, 1, 10, 1, 0) == -1
+    assert lib.moe_expert_capacity(1 << 40, 1, 1 << 30, 32, 1) == -1   # > INT32_MAX
+    assert lib.moe_expert_capacity((1 << 62), (1 << 62), 1 << 30, 1, 1) == 1 << 30
 
 
 def test_grouped_ffn_reject(lib):

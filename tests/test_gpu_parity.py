@@ -454,6 +454,78 @@ def test_grouped_ffn_all_experts_empty():
     assert torch.isnan(yp.float()).all()
 
 
+def test_row_movers_bound_rows():
+    # a caller-supplied row id at or past max_rows is never read or written:
+    # the pair is skipped, MOE_ERR_INDEX is raised, and canary rows past the
+    # buffer's max_rows keep their contents
+    T, k, D, rows, canary = 40, 2, 64, 100, 8
+    dt = torch.bfloat16
+    g = torch.Generator().manual_seed(3)
+    perm = torch.randperm(rows, generator=g)[:T * k].clone()
+    perm[5] = rows            # first row past the buffer
+    perm[70] = rows + canary - 1   # the last canary row
+    perm[9] = -1              # an ordinary drop
+    dst = perm.to(torch.int32).to(DEV)
+    ok = perm.clone()
+    ok[ok >= rows] = -1       # what the movers must treat them as
+    x = torch.randn((T, D), generator=g).to(dt)
+    gate = torch.rand((T, k), generator=g).float()
+
+    def fresh_status():
+        return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    buf = torch.full((rows + canary, D), float("nan"), dtype=dt, device=DEV)
+    st = fresh_status()
+    L.moe_permute(T, k, D, L.MOE_BF16, x.to(DEV), dst, buf, st,
+                  max_rows=rows)
+    torch.cuda.synchronize()
+    assert st.item() == L.MOE_ERR_INDEX
+    assert torch.isnan(buf[rows:].float()).all()
+    for p in range(T * k):
+        r = int(ok[p])
+        if r >= 0:
+            assert torch.equal(buf[r].cpu(), x[p // k])
+
+    yp = torch.randn((rows + canary, D), generator=g).to(dt)
+    y = torch.full((T, D), float("nan"), dtype=dt, device=DEV)
+    st = fresh_status()
+    L.moe_combine(T, k, D, L.MOE_BF16, yp.to(DEV), dst, gate.to(DEV), y, st,
+                  max_rows=rows)
+    torch.cuda.synchronize()
+    assert st.item() == L.MOE_ERR_INDEX
+    ref = O.combine(f64(yp), ok.numpy(), f64(gate), T, k)
+    assert (np.abs(f64(y) - ref) <= np.abs(ref) * 2 ** -8 + 1e-6).all()
+
+    dy = torch.randn((T, D), generator=g).to(dt).to(DEV)
+    dyp = torch.full((rows + canary, D), float("nan"), dtype=dt, device=DEV)
+    dgate = torch.full((T, k), float("nan"), device=DEV)
+    st = fresh_status()
+    L.moe_combine_backward(T, k, D, L.MOE_BF16, dy, yp.to(DEV), dst,
+                           gate.to(DEV), dyp, dgate, st, max_rows=rows)
+    torch.cuda.synchronize()
+    assert st.item() == L.MOE_ERR_INDEX
+    assert torch.isnan(dyp[rows:].float()).all()
+    dg = dgate.cpu().numpy().reshape(-1)
+    assert dg[5] == 0.0 and dg[70] == 0.0 and dg[9] == 0.0
+    assert np.isfinite(dg).all()
+
+    dx = torch.full((T, D), float("nan"), dtype=dt, device=DEV)
+    st = fresh_status()
+    L.moe_permute_backward(T, k, D, L.MOE_BF16, yp.to(DEV), dst, dx, st,
+                           max_rows=rows)
+    torch.cuda.synchronize()
+    assert st.item() == L.MOE_ERR_INDEX
+    ref = O.combine(f64(yp), ok.numpy(), np.ones((T, k)), T, k)
+    assert (np.abs(f64(dx) - ref) <= np.abs(ref) * 2 ** -8 + 1e-6).all()
+
+    # the same rows with the bad ids dropped raise nothing
+    st = fresh_status()
+    L.moe_permute(T, k, D, L.MOE_BF16, x.to(DEV), ok.to(torch.int32).to(DEV),
+                  buf, st, max_rows=rows)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+
+
 def test_empty_batch_through_every_call():
     # T = 0 through route, permute and combine: each returns MOE_OK and
     # launches nothing (the C ABI raises on any other status)

@@ -58,6 +58,10 @@ def _idx(T, k, E, seed):
     # (T, k, E, R, capacity) for two calls in a row
     [(65536, 8, 128, 8, 0), (2048, 2, 8, 8, 0)],
     [(3000, 4, 64, 16, 150), (700, 2, 16, 4, 40)],
+    # both calls on the three-kernel path that uses the scratch, the second
+    # with fewer chunks (16 against 256) and fewer experts (64 against 128):
+    # cells the first call wrote and the second does not must not leak in
+    [(65536, 8, 128, 8, 0), (4096, 8, 64, 8, 0)],
     # the largest request the 1 MiB scratch holds: 256 chunks x 1024 experts
     [(65536, 8, 1024, 32, 0), (65536, 8, 1024, 32, 300)],
 ])
