@@ -1,18 +1,27 @@
 """Benchmark of the MoE-layer forward pass on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference] [--no-cpu-baseline]
+                    [--impl ours|reference] [--no-cpu-baseline] [--only]
 
 A step is one whole layer pass (route -> dispatch layout -> permute ->
 grouped SwiGLU FFN -> combine) over one batch of seeded synthetic input with
-every input resident in HBM.  The default workload is the Mixtral-like
-top-2 layer (T=2048, D=4096, E=8, k=2, F=14336, bf16, dropless).  Between
-timed steps a 256 MiB buffer (> the 126 MB L2) is overwritten, outside the
-timed events, so every step starts with a cold L2.  After an eager warm-up,
-each of the five calls is captured as its own CUDA graph and the timed loop
-replays them back to back with events between them: the stage times are
-device time, not Python launch overhead.  The end-to-end figure ("e2e") is
-taken through the eager public API with host copies.
+every input resident in HBM.  The headline workload is the Mixtral-like
+top-2 layer (T=2048, D=4096, E=8, k=2, F=14336, bf16, dropless).  After an
+eager warm-up, one step is captured as a CUDA graph: a 256 MiB write (> the
+126 MB L2, so every step starts with a cold L2), then the five calls with
+timing events recorded inside the graph between them.  The timed loop
+replays such graphs back to back; the stage times are device time with no
+launch boundary between stages, and the flush lies outside them.  The
+end-to-end figure ("e2e") is taken through the public layer API with host
+copies.
+
+The default run also measures the other configurations the same way (the
+DeepSeek-like and Switch-like layers, the tiny fp32 layer, and the T=65536
+dispatch/combine sweep with uniform and Zipf routing) and reports each as a
+sub-record under "workloads"; --only measures --workload alone.  Tensor-bound
+kernels are reported against the measured bf16 burst peak when the timed
+region is short or never reached the power cap, else against the sustained
+one ("peak_note" says which).
 
 Rank 0 prints one JSON line.  Under torchrun (N > 1) every rank runs an
 independent replica on its own GPU with its own seed (weak scaling, no
@@ -49,23 +58,75 @@ def host_ahead():
     torch.cuda._sleep(HOST_AHEAD_CYCLES)
 
 
-def capture_stages(stages, dev):
-    """Captures each stage function (called with a stream) as its own CUDA
-    graph and returns the graphs.  The stages allocate nothing and never
-    synchronise, and the warm-up before this has set every kernel's
-    shared-memory limit."""
+GRAPH_RING = 4   # step graphs in flight (see run_step_graphs)
+
+
+def capture_step_graphs(stages, flush, dev, ring=GRAPH_RING):
+    """Captures `ring` copies of one step as CUDA graphs: the L2 flush, then
+    every stage (a function of the stream) between timing events recorded
+    inside the graph (external event-record nodes), so the stage times are
+    device time with no launch boundary between stages.  The stages
+    allocate nothing and never synchronise, and the eager warm-up before
+    this has set every kernel's shared-memory limit.  Returns a list of
+    (graph, events)."""
     import torch
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
-    graphs = []
-    for fn in stages:
+    out = []
+    for _ in range(ring):
+        evs = [torch.cuda.Event(enable_timing=True, external=True)
+               for _ in range(len(stages) + 1)]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
-            fn(s)
-        graphs.append(g)
+            flush.zero_()
+            for j, fn in enumerate(stages):
+                evs[j].record(s)
+                fn(s)
+            evs[-1].record(s)
+        out.append((g, evs))
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    return graphs
+    return out
+
+
+def run_step_graphs(graphs, K):
+    """Replays the step graphs round-robin K times on the current stream and
+    returns the stage times of every step, [K][stages] in ms.  Before a
+    graph is replayed again the host reads the times its previous replay
+    recorded, so the GPU queue stays len(graphs) - 1 steps deep and the GPU
+    never waits for the host."""
+    import torch
+    R = len(graphs)
+    times = []
+
+    def collect(evs):
+        times.append([evs[j].elapsed_time(evs[j + 1])
+                      for j in range(len(evs) - 1)])
+
+    for i in range(K):
+        g, evs = graphs[i % R]
+        if i >= R:
+            evs[-1].synchronize()
+            collect(evs)
+        g.replay()
+    torch.cuda.synchronize()
+    for i in range(max(0, K - R), K):
+        collect(graphs[i % R][1])
+    return times
+
+
+def choose_bf16_peak(peaks, wall_s, clk):
+    """The dense bf16 denominator for this run's regime: the burst figure
+    when the timed region is short (under 1 s) or the sampled clocks never
+    showed sw_power_cap, the sustained (power-capped) figure otherwise."""
+    capped = clk is not None and "sw_power_cap" in clk.get("reasons", [])
+    if wall_s < 1.0 or not capped:
+        why = (f"timed region {wall_s:.2f} s" if wall_s < 1.0 else
+               "no sw_power_cap in the sampled clocks")
+        return peaks["bf16_tflops"], f"bf16 burst ({why}), {peaks['source']}"
+    return peaks["bf16_tflops_sustained"], (
+        f"bf16 sustained (timed region {wall_s:.2f} s at sw_power_cap), "
+        f"{peaks['source']}")
 
 
 K_graph_cap = 200
@@ -231,7 +292,143 @@ def max_over_ranks(value, device, dist=None):
     return float(t.item())
 
 
-def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
+# the configurations measured beside the headline workload, each as a
+# sub-record of the default run's line
+SUB_WORKLOADS = ("deepseek_bf16", "switch_bf16", "tiny_f32",
+                 "sweep_bf16_uniform_T65536", "sweep_bf16_zipf_T65536")
+STAGES = ["route", "layout", "permute", "ffn", "combine"]
+
+
+def kernel_label(layer, key):
+    from combine_router_gemm_top_b300 import _lib as L
+    n_layout = L.moe_dispatch_layout_launches(layer.T, layer.k, layer.E)
+    return {
+        "ffn": ("moe_grouped_ffn (one tcgen05 launch, up + down)"
+                if layer.dcode == L.MOE_BF16 else
+                "moe_grouped_ffn (fp32: up and down kernels on CUDA cores)"),
+        "route": ("moe_route (one warp-per-token kernel)"
+                  if L.moe_route_launches(layer.cfg) == 1 else
+                  "moe_route (router GEMM + select)"),
+        "layout": f"moe_dispatch_layout ({n_layout} launch"
+                  f"{'es' if n_layout > 1 else ''})",
+        "permute": "moe_permute", "combine": "moe_combine"}[key]
+
+
+def measure(args, wl, dev, rank, world, local_rank, dist):
+    """Times K steps of one workload (every stage, from the step graphs) and
+    returns (record, layer, inp, extra) where record holds the throughput,
+    the per-kernel rooflines and the clocks."""
+    import torch
+    layer, inp = build_layer(wl, dev, replica_seed(wl.seed, rank))
+    x = inp["x"]
+    idx_in = inp.get("topk_idx")      # pre-drawn routing (sweep workloads)
+    gate_in = inp.get("topk_gate")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stages = [lambda s: layer.route(x, s),
+              lambda s: layer.dispatch_layout(idx_in, s),
+              lambda s: layer.permute(x, s),
+              lambda s: layer.grouped_ffn(s),
+              lambda s: layer.combine(gate_in, None, s)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        for fn in stages:
+            fn(stream)
+    torch.cuda.synchronize()
+    if layer.device_status() != 0:
+        raise RuntimeError(f"device status {layer.device_status()}")
+    graphs = capture_step_graphs(stages, flush, dev)
+    run_step_graphs(graphs, GRAPH_RING)
+    K = args.steps
+    clocks = ClockSampler(local_rank)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.5)
+    t_wall0 = time.perf_counter()
+    times = run_step_graphs(graphs, K)
+    wall = time.perf_counter() - t_wall0
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    del graphs
+    parts = {key: sum(t[j] for t in times) for j, key in enumerate(STAGES)}
+    total_ms = max_over_ranks(sum(parts.values()), dev, dist)
+    status = layer.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+    n_kept = int(layer.n_kept.item())
+    active = int((layer.expert_counts > 0).sum().item())
+    es = x.element_size()
+    peaks = load_peaks()
+    tc_peak, tc_note = choose_bf16_peak(peaks, wall, clk)
+    models = kernel_models(wl, n_kept, es, peaks, active)
+    kernels = {}
+    for key, mdl in models.items():
+        ms = parts[key] / K
+        if mdl["bound"] == "tensor":
+            ach, unit, pk = mdl["flops"] / (ms / 1e3) / 1e12, "TFLOP/s", \
+                tc_peak
+        else:
+            ach, unit, pk = mdl["bytes"] / (ms / 1e3) / 1e9, "GB/s", \
+                peaks["hbm_gbs"]
+        kernels[key] = {"ms": round(ms, 4), "bound": mdl["bound"],
+                        "achieved": round(ach, 1), "unit": unit,
+                        "frac": round(ach / pk, 4),
+                        "roofline_ms": round(mdl["roofline_ms"], 4)}
+        if mdl["flops"] and wl.dtype == "bf16":
+            kernels[key]["tflops"] = round(mdl["flops"] / (ms / 1e3) / 1e12, 1)
+    dom = max(kernels, key=lambda kk: kernels[kk]["ms"])
+    dk, dm = kernels[dom], models[dom]
+    if dk["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": dk["achieved"],
+                "peak": tc_peak, "unit": "TFLOP/s", "frac": dk["frac"],
+                "traffic": None, "peak_note": tc_note,
+                "frac_of_burst": round(dk["achieved"] / peaks["bf16_tflops"], 4),
+                "frac_of_sustained": round(
+                    dk["achieved"] / peaks["bf16_tflops_sustained"], 4),
+                "algorithmic_per_launch": dm["flops"]}
+    else:
+        roof = {"bound": "hbm", "achieved": dk["achieved"],
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dk["frac"],
+                "traffic": None, "peak_note": "HBM copy, " + peaks["source"],
+                "algorithmic_per_launch": dm["bytes"]}
+    # DRAM bytes (read + write) of one launch of the dominant kernel, from an
+    # ncu capture of the same kernel on the same workload; re-take it when
+    # the kernel changes.
+    dram = NCU_DRAM_BYTES.get((wl.name, wl.T, wl.E, dom))
+    if dram is not None:
+        roof["traffic"] = dram
+        roof["traffic_over_algorithmic"] = round(dram / dm["bytes"], 3)
+    roof["kernel"] = kernel_label(layer, dom)
+    pc_bytes = models["permute"]["bytes"] + models["combine"]["bytes"]
+    pc_ms = (parts["permute"] + parts["combine"]) / K
+    pc_gbs = pc_bytes / (pc_ms / 1e3) / 1e9
+    rec = {
+        "value": round(wl.T * world * K / (total_ms / 1e3), 1),
+        "unit": "tokens/s", "ms_per_step": round(total_ms / K, 4),
+        "steps": K,
+        "config": {"workload": wl.name, "T": wl.T, "D": wl.D, "E": wl.E,
+                   "k": wl.k, "F": wl.F, "R": wl.R,
+                   "capacity": layer.capacity or "dropless",
+                   "score": wl.score, "dtype": wl.dtype, "n_kept": n_kept,
+                   "active_experts": active,
+                   "routing": wl.routing or "router"},
+        "kernels": kernels,
+        "permute_combine": {"gbs": round(pc_gbs, 1),
+                            "frac_of_hbm": round(pc_gbs / peaks["hbm_gbs"], 4),
+                            "algorithmic_bytes": pc_bytes},
+        "roofline": roof,
+        "clocks": clk,
+        "wall_s_timed_loop": round(wall, 3)}
+    extra = dict(x=x, idx_in=idx_in, gate_in=gate_in, flush=flush,
+                 stream=stream, es=es)
+    return rec, layer, inp, extra
+
+
+def run_ours(args, rank, world, local_rank, workload=None, cpu=True,
+             subs=()):
     import torch
     from combine_router_gemm_top_b300 import workloads as W
     dist = None
@@ -246,70 +443,11 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
         wl = wl.with_(T=args.tokens)
     if args.experts:
         wl = wl.with_(E=args.experts, R=min(wl.R, args.experts))
-    layer, inp = build_layer(wl, dev, replica_seed(wl.seed, rank))
-    x = inp["x"]
-    idx_in = inp.get("topk_idx")      # pre-drawn routing (sweep workloads)
-    gate_in = inp.get("topk_gate")
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    names = ["route", "layout", "permute", "ffn", "combine"]
-
-    stages = [lambda s: layer.route(x, s),
-              lambda s: layer.dispatch_layout(idx_in, s),
-              lambda s: layer.permute(x, s),
-              lambda s: layer.grouped_ffn(s),
-              lambda s: layer.combine(gate_in, None, s)]
-    for _ in range(args.warmup):
-        flush.zero_()
-        for fn in stages:
-            fn(stream)
-    torch.cuda.synchronize()
-    if layer.device_status() != 0:
-        raise RuntimeError(f"device status {layer.device_status()}")
-    # each stage as its own CUDA graph: a replay is one cheap host call, so
-    # the host stays ahead of the GPU and the events between replays measure
-    # device time, with the GPU busy throughout (no Python launch gaps, no
-    # idle time that would lift it off its power cap)
-    graphs = capture_stages(stages, dev)
-
-    def step(m=None):
-        for j, g in enumerate(graphs):
-            if m:
-                m[j].record(stream)
-            g.replay()
-        if m:
-            m[5].record(stream)
-
-    for _ in range(3):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-
+    rec, layer, inp, ex = measure(args, wl, dev, rank, world, local_rank,
+                                  dist)
+    x, idx_in, gate_in = ex["x"], ex["idx_in"], ex["gate_in"]
+    stream, flush, es = ex["stream"], ex["flush"], ex["es"]
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    marks = [[ev() for _ in range(6)] for _ in range(args.steps)]
-    clocks = ClockSampler(local_rank)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.5)
-    t_wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        step(marks[i])
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t_wall0
-    if dist is not None:
-        dist.barrier()
-    clk = clocks.stop()
-
-    parts = dict.fromkeys(names, 0.0)
-    total_ms = 0.0
-    for m in marks:
-        for j, key in enumerate(names):
-            parts[key] += m[j].elapsed_time(m[j + 1])
-        total_ms += m[0].elapsed_time(m[5])
-    total_ms = max_over_ranks(total_ms, dev, dist)
 
     # end to end through the public layer API from pinned host memory: a
     # stream of batches, each copied in, run and copied out; copies of the
@@ -331,7 +469,7 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
     b_ev.synchronize()
     e2e_ms = max_over_ranks(a_ev.elapsed_time(b_ev), dev, dist)
 
-    # the same step replayed as one CUDA graph (launch overhead removed)
+    # the same step replayed as one CUDA graph through MoELayer.capture
     replay = layer.capture(x, idx_in, gate_in)
     for _ in range(3):
         replay()
@@ -346,99 +484,48 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
         b_ev.synchronize()
         g_ms += a_ev.elapsed_time(b_ev)
     g_ms = max_over_ranks(g_ms, dev, dist)
+    if layer.device_status() != 0:
+        raise RuntimeError(f"device status {layer.device_status()}")
+    launches = launches_per_step(layer, True) * args.steps
+    cpu_line = None
+    if rank == 0 and world == 1 and cpu and not args.no_cpu_baseline:
+        # the oracle on the host cores, fed the same (device) inputs
+        cpu_line = run_cpu_baseline(wl, inp)
+    del layer, inp, flush, ex, replay
+    torch.cuda.empty_cache()
 
-    n_kept = int(layer.n_kept.item())
-    status = layer.device_status()
-    if status != 0:
-        raise RuntimeError(f"device status {status}")
+    # the other configurations, each measured the same way
+    sub_recs = {}
+    for name in subs:
+        if name == wl.name:
+            continue
+        r, lay, inp2, ex2 = measure(args, W.WORKLOADS[name], dev, rank,
+                                    world, local_rank, dist)
+        sub_recs[name] = r
+        del lay, inp2, ex2
+        torch.cuda.empty_cache()
     if rank != 0:
         return None
 
     K = args.steps
-    es = x.element_size()
-    peaks = load_peaks()
-    tokens = wl.T * world * K
-    value = tokens / (total_ms / 1e3)
-    active = int((layer.expert_counts > 0).sum().item())
-    models = kernel_models(wl, n_kept, es, peaks, active)
-    kernels = {}
-    for key, mdl in models.items():
-        ms = parts[key] / K
-        if mdl["bound"] == "tensor":
-            ach, unit, pk = mdl["flops"] / (ms / 1e3) / 1e12, "TFLOP/s", \
-                peaks["bf16_tflops_sustained"]
-        else:
-            ach, unit, pk = mdl["bytes"] / (ms / 1e3) / 1e9, "GB/s", \
-                peaks["hbm_gbs"]
-        kernels[key] = {"ms": round(ms, 4), "bound": mdl["bound"],
-                        "achieved": round(ach, 1), "unit": unit,
-                        "frac": round(ach / pk, 4),
-                        "roofline_ms": round(mdl["roofline_ms"], 4)}
-        if mdl["flops"] and wl.dtype == "bf16":
-            kernels[key]["tflops"] = round(mdl["flops"] / (ms / 1e3) / 1e12, 1)
-    dom = max(kernels, key=lambda kk: kernels[kk]["ms"])
-    dk, dm = kernels[dom], models[dom]
-    if dk["bound"] == "tensor":
-        roof = {"bound": "tensor", "achieved": dk["achieved"],
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": dk["frac"], "traffic": None,
-                "peak_note": "bf16 sustained (seconds-long loop), "
-                             + peaks["source"],
-                "frac_of_burst": round(dk["achieved"] / peaks["bf16_tflops"], 4),
-                "algorithmic_per_launch": dm["flops"]}
-    else:
-        roof = {"bound": "hbm", "achieved": dk["achieved"],
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dk["frac"],
-                "traffic": None, "peak_note": "HBM copy, " + peaks["source"],
-                "algorithmic_per_launch": dm["bytes"]}
-    # DRAM bytes (read + write) of one launch of the dominant kernel, from an
-    # ncu capture of the same kernel on the same workload; re-take it when
-    # the kernel changes.
-    dram = NCU_DRAM_BYTES.get((wl.name, wl.T, wl.E, dom))
-    if dram is not None:
-        roof["traffic"] = dram
-        roof["traffic_over_algorithmic"] = round(
-            dram / (dm["bytes"] if dk["bound"] == "hbm" else
-                    models[dom]["bytes"]), 3)
-    from combine_router_gemm_top_b300 import _lib as L
-    n_layout = L.moe_dispatch_layout_launches(layer.T, layer.k, layer.E)
-    roof["kernel"] = {
-        "ffn": ("moe_grouped_ffn (one tcgen05 launch, up + down)"
-                if layer.dcode == L.MOE_BF16 else
-                "moe_grouped_ffn (fp32: up and down kernels on CUDA cores)"),
-        "route": ("moe_route (one warp-per-token kernel)"
-                  if L.moe_route_launches(layer.cfg) == 1 else
-                  "moe_route (router GEMM + select)"),
-        "layout": f"moe_dispatch_layout ({n_layout} launch"
-                  f"{'es' if n_layout > 1 else ''})",
-        "permute": "moe_permute", "combine": "moe_combine"}[dom]
-    pc_bytes = models["permute"]["bytes"] + models["combine"]["bytes"]
-    pc_ms = (parts["permute"] + parts["combine"]) / K
-    pc_gbs = pc_bytes / (pc_ms / 1e3) / 1e9
     e2e_tokens_s = wl.T * world * e2e_steps / (e2e_ms / 1e3)
+    cfg = dict(rec["config"])
+    cfg.update({"parallelism": f"replicas x{world}",
+                "l2": "flushed (256 MiB write) before every timed step",
+                "launch": "each step one CUDA graph with timing events "
+                          "between its stages: stage times are device time"})
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "metric": METRIC, "value": rec["value"], "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": round(total_ms / K, 4), "higher_is_better": True,
+        "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == "bf16" else "f32",
         "data": "synthetic (seeded; random-init weights of the stated "
                 "shapes)",
-        "config": {"workload": wl.name, "T": wl.T, "D": wl.D, "E": wl.E,
-                   "k": wl.k, "F": wl.F, "R": wl.R,
-                   "capacity": layer.capacity or "dropless",
-                   "score": wl.score, "n_kept": n_kept,
-                   "active_experts": active,
-                   "routing": wl.routing or "router",
-                   "parallelism": f"replicas x{world}",
-                   "l2": "flushed (256 MiB write) before every timed step",
-                   "launch": "each stage replayed as its own CUDA graph, "
-                             "back to back: stage times are device time"},
-        "kernels": kernels,
-        "permute_combine": {"gbs": round(pc_gbs, 1),
-                            "frac_of_hbm": round(pc_gbs / peaks["hbm_gbs"], 4),
-                            "algorithmic_bytes": pc_bytes},
-        "roofline": roof,
+        "config": cfg,
+        "kernels": rec["kernels"],
+        "permute_combine": rec["permute_combine"],
+        "roofline": rec["roofline"],
         "e2e": {"value": round(e2e_tokens_s, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": wl.T * wl.D * es,
                 "d2h_bytes_per_step": wl.T * wl.D * es,
@@ -452,15 +539,13 @@ def run_ours(args, rank, world, local_rank, workload=None, cpu=True):
                   "steps": g_steps,
                   "how": "MoELayer.capture: the whole step as one CUDA "
                          "graph, L2 flushed before every replay"},
-        "gpu_launches": launches_per_step(layer, True) * K,
-        "clocks": clk,
-        "wall_s_timed_loop": round(wall, 3),
+        "gpu_launches": launches,
+        "clocks": rec["clocks"],
+        "wall_s_timed_loop": rec["wall_s_timed_loop"],
     }
-    if world == 1 and cpu and not args.no_cpu_baseline:
-        # the oracle on the host cores, fed the same (device) inputs
-        line["cpu_baseline"] = run_cpu_baseline(wl, inp)
-    del layer, inp, flush
-    torch.cuda.empty_cache()
+    if sub_recs:
+        line["workloads"] = sub_recs
+    line["cpu_baseline"] = cpu_line
     return line
 
 
@@ -817,6 +902,9 @@ def main():
                     help="time router statistics, the bias step, the "
                          "dispatch matrix and the padded static-capacity "
                          "path: one JSON line per workload")
+    ap.add_argument("--only", action="store_true",
+                    help="measure --workload alone (no sub-records of the "
+                         "other configurations)")
     ap.add_argument("--sweep", action="store_true",
                     help="dispatch/combine bandwidth sweep: one JSON line "
                          "per (T, routing) identity-expert workload")
@@ -853,9 +941,9 @@ def main():
                     if ln is not None:
                         print(json.dumps(ln), flush=True)
             return
-        line = run_ours(args, rank, world, local_rank)
-        if line is not None and "cpu_baseline" not in line:
-            line["cpu_baseline"] = None
+        subs = () if (args.only or args.tokens or args.experts) else \
+            SUB_WORKLOADS
+        line = run_ours(args, rank, world, local_rank, subs=subs)
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1 and args.impl == "ours":

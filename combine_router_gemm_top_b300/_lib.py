@@ -86,7 +86,7 @@ _SIGS = {
                            _vp]),
     "moe_grouped_ffn_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "moe_grouped_ffn": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
-                               _vp, _vp, _vp, _sz, _vp, _vp]),
+                               _vp, _vp, _vp, _sz, _i32, _vp, _vp]),
     "moe_combine": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32,
                            _vp, _vp]),
     "moe_expert_capacity": (_i32, [ctypes.c_int64, ctypes.c_int64, _i32, _i32,
@@ -257,11 +257,12 @@ def moe_grouped_ffn_workspace_size(E, D, F, max_rows, dtype) -> int:
 
 
 def moe_grouped_ffn(E, D, F, max_rows, dtype, xp, expert_offsets, w13, w2,
-                    yp, workspace, status, stream=None):
+                    yp, workspace, status, stream=None, max_ctas=0):
     nbytes = workspace.numel() * workspace.element_size()
     _check(load().moe_grouped_ffn(E, D, F, max_rows, dtype, _p(xp),
                                   _p(expert_offsets), _p(w13), _p(w2),
-                                  _p(yp), _p(workspace), nbytes, _p(status),
+                                  _p(yp), _p(workspace), nbytes,
+                                  int(max_ctas), _p(status),
                                   _stream(stream)), "moe_grouped_ffn")
 
 

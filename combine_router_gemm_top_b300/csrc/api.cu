@@ -239,8 +239,8 @@ moe_status moe_grouped_ffn(int32_t E, int32_t D, int32_t F, int32_t max_rows,
                            int32_t dtype, const void* xp,
                            const int32_t* expert_offsets, const void* w13,
                            const void* w2, void* yp, void* workspace,
-                           size_t workspace_bytes, int32_t* status,
-                           moe_stream_t stream) {
+                           size_t workspace_bytes, int32_t max_ctas,
+                           int32_t* status, moe_stream_t stream) {
   if (E < 1 || D <= 0 || F <= 0 || max_rows < 0 || !valid_dtype(dtype))
     return MOE_ERR_INVALID;
   if (max_rows == 0) return MOE_OK;
@@ -263,7 +263,7 @@ moe_status moe_grouped_ffn(int32_t E, int32_t D, int32_t F, int32_t max_rows,
       return MOE_ERR_INVALID;
   }
   return launch_grouped_ffn(E, D, F, max_rows, dtype, xp, expert_offsets, w13,
-                            w2, yp, workspace, status,
+                            w2, yp, workspace, max_ctas, status,
                             reinterpret_cast<cudaStream_t>(stream), num_sms());
 }
 

@@ -94,8 +94,8 @@ size_t ffn_ws_bytes(int E, int D, int F, int max_rows, int dtype) {
 moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
                               const void* xp, const int32_t* offsets,
                               const void* w13, const void* w2, void* yp,
-                              void* ws, int32_t* status, cudaStream_t stream,
-                              int num_sms) {
+                              void* ws, int max_ctas, int32_t* status,
+                              cudaStream_t stream, int num_sms) {
   if (max_rows == 0) return MOE_OK;
   if (dtype == MOE_F32) {
     float* h = static_cast<float*>(ws);
@@ -161,9 +161,34 @@ moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
                            227 * 1024, &attr_done))
     return MOE_ERR_CUDA;
   const size_t smem = umma_gemm_smem_bytes(up.BN, up.stages);
-  umma_ffn_kernel<<<num_sms, kGemmThreads, smem, stream>>>(tm_xp, tm_w13, tm_h,
-                                                          tm_w2, f);
-  return launch_status();
+  // Down tiles wait for up tiles that other CTAs own, so every CTA of the
+  // grid must be resident at once: a cooperative launch guarantees that (or
+  // fails to launch), whatever else runs on the device.  One CTA per SM at
+  // most, fewer when the caller asks.
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, umma_ffn_kernel, kGemmThreads, smem) != cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  const int grid = max_ctas > 0 && max_ctas < num_sms ? max_ctas : num_sms;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, umma_ffn_kernel, tm_xp, tm_w13, tm_h, tm_w2,
+                         f) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
 // ----------------------------------------------------------- self-test

@@ -73,8 +73,8 @@ size_t ffn_ws_bytes(int E, int D, int F, int max_rows, int dtype);
 moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
                               const void* xp, const int32_t* offsets,
                               const void* w13, const void* w2, void* yp,
-                              void* ws, int32_t* status, cudaStream_t stream,
-                              int num_sms);
+                              void* ws, int max_ctas, int32_t* status,
+                              cudaStream_t stream, int num_sms);
 
 size_t router_stats_ws_bytes(int T, int E);
 moe_status launch_router_stats(int T, int E, int k, int score,

@@ -254,16 +254,23 @@ MOE_API size_t moe_grouped_ffn_workspace_size(int32_t E, int32_t D, int32_t F,
  *   w2      [E, D, F] dtype, K-major; 256-byte aligned
  *   yp      [max_rows, D] dtype out; rows >= expert_offsets[E] untouched
  *   max_rows  rows allocated in xp / yp (>= expert_offsets[E]; T*k works)
+ *   max_ctas  MOE_BF16: at most this many CTAs (one per SM); <= 0 means one
+ *             per SM of the device.  Fewer leave SMs to other streams.
  * Expert offsets are read on the device: no host synchronisation.
  * MOE_BF16 runs on the tcgen05 tensor cores with fp32 accumulation and
- * needs D % 64 == 0 and F % 128 == 0 (else MOE_ERR_UNSUPPORTED);
- * MOE_F32 runs fp32 FMA. */
+ * needs D % 64 == 0 and F % 128 == 0 (else MOE_ERR_UNSUPPORTED).  It is one
+ * persistent launch for both projections in which tiles of the down
+ * projection wait (bounded) for the up-projection tiles of their rows held
+ * by other CTAs; the launch is cooperative, so CUDA makes every CTA
+ * resident at once, and a device that cannot host the grid fails the call
+ * with MOE_ERR_CUDA instead of stalling.  MOE_F32 runs fp32 FMA (max_ctas
+ * unused). */
 MOE_API moe_status moe_grouped_ffn(int32_t E, int32_t D, int32_t F, int32_t max_rows,
                            int32_t dtype, const void* xp,
                            const int32_t* expert_offsets, const void* w13,
                            const void* w2, void* yp, void* workspace,
-                           size_t workspace_bytes, int32_t* status,
-                           moe_stream_t stream);
+                           size_t workspace_bytes, int32_t max_ctas,
+                           int32_t* status, moe_stream_t stream);
 
 /* moe_combine -- y[t] = sum over kept slots j of
  * topk_gate[t, j] * yp[dst_row[t*k + j]], accumulated in fp32 in slot

@@ -183,19 +183,19 @@ def test_expert_capacity_matches_the_oracle(lib):
 def test_grouped_ffn_reject(lib):
     ok_ws = 1 << 40
     assert lib.moe_grouped_ffn(8, 100, 256, 64, L.MOE_BF16, FAKE, FAKE, FAKE,
-                               FAKE, FAKE, FAKE, ok_ws, None, None) == \
+                               FAKE, FAKE, FAKE, ok_ws, 0, None, None) == \
         L.MOE_ERR_UNSUPPORTED                          # D % 64
     assert lib.moe_grouped_ffn(8, 128, 200, 64, L.MOE_BF16, FAKE, FAKE, FAKE,
-                               FAKE, FAKE, FAKE, ok_ws, None, None) == \
+                               FAKE, FAKE, FAKE, ok_ws, 0, None, None) == \
         L.MOE_ERR_UNSUPPORTED                          # F % 128
     assert lib.moe_grouped_ffn(8, 128, 256, 64, L.MOE_BF16, FAKE + 16, FAKE,
-                               FAKE, FAKE, FAKE, FAKE, ok_ws, None, None) == \
+                               FAKE, FAKE, FAKE, FAKE, ok_ws, 0, None, None) == \
         L.MOE_ERR_INVALID                              # TMA base alignment
     assert lib.moe_grouped_ffn(8, 128, 256, 64, L.MOE_BF16, FAKE, FAKE, FAKE,
-                               FAKE, FAKE, FAKE, 16, None, None) == \
+                               FAKE, FAKE, FAKE, 16, 0, None, None) == \
         L.MOE_ERR_INVALID                              # workspace too small
     assert lib.moe_grouped_ffn(8, 128, 256, 64, L.MOE_BF16, FAKE, None, FAKE,
-                               FAKE, FAKE, FAKE, ok_ws, None, None) == \
+                               FAKE, FAKE, FAKE, ok_ws, 0, None, None) == \
         L.MOE_ERR_INVALID
     # H [max_rows, F], then one counter per row block (ceil(64/128) + E)
     assert lib.moe_grouped_ffn_workspace_size(8, 128, 256, 64, L.MOE_BF16) == \

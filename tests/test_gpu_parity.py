@@ -379,7 +379,7 @@ def test_permute_combine_parity(T, k, E, D, dt, cap):
 
 
 # ------------------------------------------------------------ grouped FFN
-def run_ffn(xp, counts, w13, w2, F, sentinel=True):
+def run_ffn(xp, counts, w13, w2, F, sentinel=True, max_ctas=0):
     E = len(counts)
     D = xp.shape[1]
     max_rows = xp.shape[0]
@@ -393,7 +393,7 @@ def run_ffn(xp, counts, w13, w2, F, sentinel=True):
         device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     L.moe_grouped_ffn(E, D, F, max_rows, L.dtype_code(dt), xp.to(DEV), d_off,
-                      w13.to(DEV), w2.to(DEV), yp, ws, st)
+                      w13.to(DEV), w2.to(DEV), yp, ws, st, max_ctas=max_ctas)
     torch.cuda.synchronize()
     assert st.item() == 0
     return yp, off
@@ -441,6 +441,26 @@ def test_grouped_ffn_parity(case):
     assert np.isfinite(got).all()
     assert rel_err(got, ref) <= tol_for(dt)
     assert torch.isnan(yp[n:].float()).all()
+
+
+@pytest.mark.parametrize("ctas", [1, 8, 37])
+def test_grouped_ffn_on_few_ctas(ctas):
+    # the persistent launch on a grid far below the SM count: every CTA walks
+    # many up tiles and then down tiles that wait for up tiles other CTAs
+    # hold; the result must not depend on the grid, and it must finish well
+    # inside the bounded waits (no MOE_ERR_TIMEOUT)
+    E, D, F, counts = 4, 1024, 512, [300, 40, 0, 129]
+    n = sum(counts)
+    g = torch.Generator().manual_seed(91)
+    xp = torch.randn((n + 5, D), generator=g).to(torch.bfloat16)
+    std = 1.0 / math.sqrt(D)
+    w13 = (torch.randn((E, 2 * F, D), generator=g) * std).to(torch.bfloat16)
+    w2 = (torch.randn((E, D, F), generator=g) * std).to(torch.bfloat16)
+    yp, off = run_ffn(xp, counts, w13, w2, F, max_ctas=ctas)
+    ref = O.grouped_ffn(f64(xp)[:n], off, f64(w13), f64(w2))
+    assert rel_err(f64(yp[:n]), ref) <= 1e-2
+    full, _ = run_ffn(xp, counts, w13, w2, F)
+    assert torch.equal(yp[:n], full[:n])    # the same bits on every grid
 
 
 def test_grouped_ffn_all_experts_empty():
