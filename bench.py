@@ -635,6 +635,25 @@ def run_extras(args, local_rank, workload):
     put("dispatch_matrix", timed(lambda: L.moe_dispatch_matrix(
         T, k, E, R, R, layer.topk_idx, layer.dst_row, mat, st)),
         nbytes=2 * P * 4)
+    # micro-batches: four batches of T tokens one after another, and the
+    # same four with the routing, layout and permute of batch i+1 on a
+    # second stream while batch i's experts (on all SMs but 8) and combine
+    # run (MoELayer.forward_overlapped)
+    if not layer.identity:
+        n_mb = 4
+        xs = [x] * n_mb
+        ys = [torch.empty_like(x) for _ in range(n_mb)]
+
+        def sequential():
+            for xi, yi in zip(xs, ys):
+                layer.forward(xi, y=yi)
+        layer.forward_overlapped(xs, ys)      # builds the twin buffers
+        put("microbatches_sequential", timed(sequential))
+        put("microbatches_overlapped",
+            timed(lambda: layer.forward_overlapped(xs, ys)))
+        out["microbatches_overlapped"]["gain_vs_sequential"] = round(
+            out["microbatches_sequential"]["ms"] /
+            out["microbatches_overlapped"]["ms"] - 1.0, 4)
     cap = layer.capacity
     if cap > 0 and not layer.identity:
         rows = E * cap

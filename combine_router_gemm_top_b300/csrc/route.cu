@@ -78,111 +78,102 @@ __device__ __forceinline__ int group_of(int e, float inv_gs) {
 constexpr int kSelWarps = 8;
 constexpr int kSelGroupTop = 8;   // per-lane scan handles group_score_topk <= 8
 
-// Selection for one token, one warp: lane l holds the logits of experts
-// e = l + 32*i, i < NI, in lg; sk is the warp's shared scratch for the
-// group scan.  Writes the token's ids and gates (and logits when asked).
+// Lane g < n_groups: the fp32 sum of the m largest keys of group g (added
+// largest first) and the m-th largest key; keys of experts e = lane + 32 i
+// in key[] (-inf for none).  Lane g scans its group's keys from the warp's
+// shared scratch keeping the m largest in a sorted list (m <= 8; equal keys
+// are interchangeable for the sum).
 template <int NI>
-__device__ __forceinline__ void select_token(const RouteSelectArgs& a,
-                                             int64_t t, int lane,
-                                             float (&lg)[NI], float* sk) {
-  const int E = a.E;
-  float key[NI];
-  uint32_t code[NI];
+__device__ __forceinline__ void group_top(const float (&key)[NI], int lane,
+                                          int E, int n_groups, int gs, int m,
+                                          float* sk, float& sum, float& mth) {
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int e = lane + 32 * i;
-    if (e < E) {
-      if (a.logit_offset != nullptr) lg[i] = __fadd_rn(lg[i], a.logit_offset[e]);
-      if (a.logits_out != nullptr) a.logits_out[t * E + e] = lg[i];
-      float k = lg[i];
-      if (a.score == MOE_SCORE_SIGMOID_BIAS) {
-        k = sigmoid_score(k);
-        if (a.sel_bias != nullptr) k = __fadd_rn(k, a.sel_bias[e]);
+    if (e < E) sk[e + (e >> 5)] = key[i];
+  }
+  __syncwarp();
+  sum = 0.0f;
+  mth = -INFINITY;
+  if (lane < n_groups) {
+    float v[kSelGroupTop];
+#pragma unroll
+    for (int j = 0; j < kSelGroupTop; ++j) v[j] = -INFINITY;
+    for (int e = lane * gs; e < (lane + 1) * gs; ++e) {
+      float x = sk[e + (e >> 5)];
+#pragma unroll
+      for (int j = 0; j < kSelGroupTop; ++j) {
+        const float hi = fmaxf(v[j], x);
+        x = fminf(v[j], x);
+        v[j] = hi;
       }
-      key[i] = k;
-      code[i] = key_code(k);
-    } else {
-      key[i] = 0.0f;
-      code[i] = 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kSelGroupTop; ++j) {
+      if (j < m) sum = __fadd_rn(sum, v[j]);
+      if (j == m - 1) mth = v[j];
     }
   }
+  __syncwarp();
+}
 
-  // group-limited selection: score each group by the sum of its
-  // group_score_topk largest keys (added largest first), keep the
-  // topk_groups best groups (lower group index on equal scores)
-  if (a.n_groups > 1) {
-    const int gs = E / a.n_groups;
-    const float inv_gs = 1.0f / static_cast<float>(gs);
-    const int m = a.group_score_topk;
-    float gscore = 0.0f;   // lane g < n_groups: group g's score
-    if (m <= kSelGroupTop) {
-      // lane g scans its group's keys, keeping the m largest in a sorted
-      // list; equal keys are interchangeable for the sum
+// Lane g < n_groups: the fp32 sum of the m largest keys of group g by m
+// warp-wide arg-max rounds per group (any m).
+template <int NI>
+__device__ __forceinline__ float group_sum_rounds(const float (&key)[NI],
+                                                  const uint32_t (&code)[NI],
+                                                  int lane, int n_groups,
+                                                  float inv_gs, int m) {
+  float gscore = 0.0f;
+  for (int g = 0; g < n_groups; ++g) {
+    uint32_t c[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+      c[i] = group_of(lane + 32 * i, inv_gs) == g ? code[i] : 0u;
+    float acc = 0.0f;   // the same on every lane, largest key first
+    for (int j = 0; j < m; ++j) {
+      const int w = warp_argmax<NI>(c, lane);
+      float mine = 0.0f;
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) sk[e + (e >> 5)] = key[i];
-      }
-      __syncwarp();
-      if (lane < a.n_groups) {
-        float v[kSelGroupTop];
-#pragma unroll
-        for (int j = 0; j < kSelGroupTop; ++j) v[j] = -INFINITY;
-        for (int e = lane * gs; e < (lane + 1) * gs; ++e) {
-          float x = sk[e + (e >> 5)];
-#pragma unroll
-          for (int j = 0; j < kSelGroupTop; ++j) {
-            const float hi = fmaxf(v[j], x);
-            x = fminf(v[j], x);
-            v[j] = hi;
-          }
+        if (lane + 32 * i == w) {
+          mine = key[i];
+          c[i] = 0u;
         }
-#pragma unroll
-        for (int j = 0; j < kSelGroupTop; ++j)
-          if (j < m) gscore = __fadd_rn(gscore, v[j]);
       }
-    } else {
-      // larger m: m warp-wide arg-max rounds per group
-      for (int g = 0; g < a.n_groups; ++g) {
-        uint32_t c[NI];
-#pragma unroll
-        for (int i = 0; i < NI; ++i)
-          c[i] = group_of(lane + 32 * i, inv_gs) == g ? code[i] : 0u;
-        float acc = 0.0f;   // the same on every lane, largest key first
-        for (int j = 0; j < m; ++j) {
-          const int w = warp_argmax<NI>(c, lane);
-          float mine = 0.0f;
-#pragma unroll
-          for (int i = 0; i < NI; ++i) {
-            if (lane + 32 * i == w) {
-              mine = key[i];
-              c[i] = 0u;
-            }
-          }
-          acc = __fadd_rn(acc, __shfl_sync(0xffffffffu, mine, w & 31));
-        }
-        if (lane == g) gscore = acc;
-      }
+      acc = __fadd_rn(acc, __shfl_sync(0xffffffffu, mine, w & 31));
     }
-    uint32_t gc[1] = {lane < a.n_groups ? key_code(gscore) : 0u};
-    uint32_t chosen = 0;
-    for (int j = 0; j < a.topk_groups; ++j) {
-      const int w = warp_argmax<1>(gc, lane);
-      if (w < 0) break;
-      chosen |= 1u << w;
-      if (lane == w) gc[0] = 0u;
-    }
-#pragma unroll
-    for (int i = 0; i < NI; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((chosen >> group_of(e, inv_gs)) & 1u)) code[i] = 0u;
-    }
+    if (lane == g) gscore = acc;
   }
+  return gscore;
+}
 
-  // top-k by repeated warp arg-max; lane j keeps slot j
-  int my_idx = -1;
-  float my_logit = 0.0f;
-  for (int j = 0; j < a.k; ++j) {
+// The topk_groups best groups by score (lower group index on equal scores)
+// as a bit mask, from lane g's score of group g.
+__device__ __forceinline__ uint32_t choose_groups(float gscore, int lane,
+                                                  int n_groups,
+                                                  int topk_groups) {
+  uint32_t gc[1] = {lane < n_groups ? key_code(gscore) : 0u};
+  uint32_t chosen = 0;
+  for (int j = 0; j < topk_groups; ++j) {
+    const int w = warp_argmax<1>(gc, lane);
+    if (w < 0) break;
+    chosen |= 1u << w;
+    if (lane == w) gc[0] = 0u;
+  }
+  return chosen;
+}
+
+// top-k by repeated warp arg-max over code[]: lane j < k receives slot j's
+// expert and its logit.
+template <int NI>
+__device__ __forceinline__ void topk_rounds(uint32_t (&code)[NI],
+                                            const float (&lg)[NI], int k,
+                                            int lane, int& my_idx,
+                                            float& my_logit) {
+  my_idx = -1;
+  my_logit = 0.0f;
+  for (int j = 0; j < k; ++j) {
     const int w = warp_argmax<NI>(code, lane);
     float mine = 0.0f;
 #pragma unroll
@@ -198,6 +189,244 @@ __device__ __forceinline__ void select_token(const RouteSelectArgs& a,
       my_logit = wl;
     }
   }
+}
+
+// Softmax modes: the key is the logit itself.
+template <int NI>
+__device__ __forceinline__ void select_by_logit(const RouteSelectArgs& a,
+                                                int lane, const float (&lg)[NI],
+                                                float* sk, int& my_idx,
+                                                float& my_logit) {
+  const int E = a.E;
+  float key[NI];
+  uint32_t code[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const bool in = lane + 32 * i < E;
+    key[i] = in ? lg[i] : -INFINITY;
+    code[i] = in ? key_code(lg[i]) : 0u;
+  }
+  if (a.n_groups > 1) {
+    const int gs = E / a.n_groups;
+    const float inv_gs = 1.0f / static_cast<float>(gs);
+    const int m = a.group_score_topk;
+    float gscore, mth;
+    if (m <= kSelGroupTop)
+      group_top<NI>(key, lane, E, a.n_groups, gs, m, sk, gscore, mth);
+    else
+      gscore = group_sum_rounds<NI>(key, code, lane, a.n_groups, inv_gs, m);
+    const uint32_t chosen = choose_groups(gscore, lane, a.n_groups,
+                                          a.topk_groups);
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((chosen >> group_of(e, inv_gs)) & 1u)) code[i] = 0u;
+    }
+  }
+  topk_rounds<NI>(code, lg, a.k, lane, my_idx, my_logit);
+}
+
+// fp32 approximation of the sigmoid score: expf (within 2 ulp), one add and
+// one division, so it lies within 3.5 * 2^-24 of fp32(sigmoid(l)), and an
+// approximate key fp32(approx + b) within 2^-21.5 (1 + |b|) of the exact
+// key.  The selection uses it only to rule experts out, with a margin four
+// times that bound.
+__device__ __forceinline__ float sigmoid_approx(float l) {
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
+}
+constexpr float kSigmoidKeySlack = 1.0f / 524288.0f;   // 2^-19
+
+// Exact keys fp32(sigmoid_score(l) + b_e) of the experts flagged in need[]
+// (this lane's slots), spread over the warp: the flagged experts are
+// numbered slot by slot, lane by lane, and candidate c is evaluated by lane
+// c mod 32 in round c / 32, so the float64 work is not left to the lanes
+// that happen to own the candidates.
+template <int NI>
+__device__ __forceinline__ void exact_sigmoid_keys(const RouteSelectArgs& a,
+                                                   int lane,
+                                                   const float (&lg)[NI],
+                                                   const bool (&need)[NI],
+                                                   float (&key)[NI]) {
+  uint32_t mask[NI];
+  int base[NI];
+  int total = 0;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    mask[i] = __ballot_sync(0xffffffffu, need[i]);
+    base[i] = total;
+    total += __popc(mask[i]);
+  }
+  const uint32_t below = (1u << lane) - 1u;
+  for (int r0 = 0; r0 < total; r0 += 32) {
+    const int c = r0 + lane;   // the candidate this lane evaluates
+    float l = 0.0f;
+    int e = -1;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int n = c - base[i];
+      const bool mine = n >= 0 && n < __popc(mask[i]);
+      int owner = 0;
+      if (mine) {
+        uint32_t mm = mask[i];
+        for (int q = 0; q < n; ++q) mm &= mm - 1u;   // drop the n lowest
+        owner = __ffs(mm) - 1;
+      }
+      const float v = __shfl_sync(0xffffffffu, lg[i], owner);
+      if (mine) {
+        l = v;
+        e = owner + 32 * i;
+      }
+    }
+    float kx = 0.0f;
+    if (e >= 0) {
+      kx = sigmoid_score(l);
+      if (a.sel_bias != nullptr) kx = __fadd_rn(kx, a.sel_bias[e]);
+    }
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int cc = base[i] + __popc(mask[i] & below);   // (lane, i)'s number
+      const bool here = need[i] && cc >= r0 && cc < r0 + 32;
+      const float v = __shfl_sync(0xffffffffu, kx, here ? cc - r0 : 0);
+      if (here) key[i] = v;
+    }
+  }
+}
+
+// Sigmoid mode: key = fp32(fp32(sigmoid(l)) + b_e), the sigmoid in float64.
+// Every expert gets the cheap approximate key; exact keys are evaluated only
+// for the experts that can still matter.  An expert whose approximate key
+// is more than twice the error bound below the m-th largest approximate key
+// of its group (or the k-th largest among the eligible experts) lies below
+// at least m (or k) experts whatever the exact keys are, so it can neither
+// add to its group's score nor be selected, ties included.
+template <int NI>
+__device__ __forceinline__ void select_by_sigmoid(const RouteSelectArgs& a,
+                                                  int lane,
+                                                  const float (&lg)[NI],
+                                                  float* sk, int& my_idx,
+                                                  float& my_logit) {
+  const int E = a.E;
+  float ka[NI], key[NI];
+  bool elig[NI], exact[NI], need[NI];
+  float bmax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int e = lane + 32 * i;
+    elig[i] = e < E;
+    exact[i] = false;
+    float b = 0.0f;
+    if (elig[i] && a.sel_bias != nullptr) b = a.sel_bias[e];
+    ka[i] = elig[i] ? __fadd_rn(sigmoid_approx(lg[i]), b) : -INFINITY;
+    key[i] = ka[i];
+    bmax = fmaxf(bmax, fabsf(b));
+  }
+  bmax = warp_max(bmax);
+  const float slack = 2.0f * kSigmoidKeySlack * (1.0f + bmax);
+
+  if (a.n_groups > 1) {
+    const int gs = E / a.n_groups;
+    const float inv_gs = 1.0f / static_cast<float>(gs);
+    const int m = a.group_score_topk;
+    float gscore, mth;
+    if (m <= kSelGroupTop) {
+      // exact keys for each group's candidates, then the exact group scores
+      // from those alone
+      group_top<NI>(ka, lane, E, a.n_groups, gs, m, sk, gscore, mth);
+      const float thr_own = mth - slack;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        const int g = group_of(lane + 32 * i, inv_gs);
+        const float thr = __shfl_sync(0xffffffffu, thr_own, g & 31);
+        need[i] = elig[i] && ka[i] >= thr;
+      }
+      exact_sigmoid_keys<NI>(a, lane, lg, need, key);
+      float kc[NI];
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        exact[i] = need[i];
+        kc[i] = exact[i] ? key[i] : -INFINITY;
+      }
+      group_top<NI>(kc, lane, E, a.n_groups, gs, m, sk, gscore, mth);
+    } else {
+      // wider group scores: exact keys for every expert
+#pragma unroll
+      for (int i = 0; i < NI; ++i) need[i] = elig[i];
+      exact_sigmoid_keys<NI>(a, lane, lg, need, key);
+      uint32_t code[NI];
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        exact[i] = elig[i];
+        code[i] = elig[i] ? key_code(key[i]) : 0u;
+      }
+      gscore = group_sum_rounds<NI>(key, code, lane, a.n_groups, inv_gs, m);
+    }
+    const uint32_t chosen = choose_groups(gscore, lane, a.n_groups,
+                                          a.topk_groups);
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+      if (elig[i] && !((chosen >> group_of(lane + 32 * i, inv_gs)) & 1u))
+        elig[i] = false;
+  }
+
+  // the k-th largest approximate key among the eligible experts
+  uint32_t ca[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) ca[i] = elig[i] ? key_code(ka[i]) : 0u;
+  float tk = -INFINITY;
+  for (int j = 0; j < a.k; ++j) {
+    const int w = warp_argmax<NI>(ca, lane);
+    if (w < 0) {
+      tk = -INFINITY;   // fewer than k eligible: all of them stay
+      break;
+    }
+    float mine = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      if (lane + 32 * i == w) {
+        mine = ka[i];
+        ca[i] = 0u;
+      }
+    }
+    tk = __shfl_sync(0xffffffffu, mine, w & 31);
+  }
+  const float thr = tk - slack;
+  uint32_t code[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const bool cand = elig[i] && ka[i] >= thr;
+    need[i] = cand && !exact[i];
+  }
+  exact_sigmoid_keys<NI>(a, lane, lg, need, key);
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const bool cand = elig[i] && ka[i] >= thr;
+    code[i] = cand ? key_code(key[i]) : 0u;
+  }
+  topk_rounds<NI>(code, lg, a.k, lane, my_idx, my_logit);
+}
+
+// Selection for one token, one warp: lane l holds the logits of experts
+// e = l + 32*i, i < NI, in lg; sk is the warp's shared scratch for the
+// group scan.  Writes the token's ids and gates (and logits when asked).
+template <int NI>
+__device__ __forceinline__ void select_token(const RouteSelectArgs& a,
+                                             int64_t t, int lane,
+                                             float (&lg)[NI], float* sk) {
+  const int E = a.E;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      if (a.logit_offset != nullptr) lg[i] = __fadd_rn(lg[i], a.logit_offset[e]);
+      if (a.logits_out != nullptr) a.logits_out[t * E + e] = lg[i];
+    }
+  }
+  int my_idx;
+  float my_logit;
+  if (a.score == MOE_SCORE_SIGMOID_BIAS)
+    select_by_sigmoid<NI>(a, lane, lg, sk, my_idx, my_logit);
+  else
+    select_by_logit<NI>(a, lane, lg, sk, my_idx, my_logit);
 
   // gates
   const bool slot = lane < a.k;

@@ -56,6 +56,12 @@ class MoELayer:
                  group_score_topk=0, device=None, keep_logits=False,
                  padded=False):
         L.load()
+        self._init_args = dict(
+            T=T, D=D, E=E, k=k, R=R, F=F, score=score,
+            capacity_factor=capacity_factor, n_groups=n_groups,
+            topk_groups=topk_groups, group_score_topk=group_score_topk,
+            device=device, keep_logits=keep_logits, padded=padded)
+        self.ffn_ctas = 0   # CTAs of the grouped FFN; 0 = one per SM
         self.device = torch.device(device or w_r.device)
         self.dtype = w_r.dtype
         self.dcode = L.dtype_code(self.dtype)
@@ -141,7 +147,8 @@ class MoELayer:
             return
         L.moe_grouped_ffn(self.E, self.D, self.F, self.T * self.k, self.dcode,
                           self.xp, self.expert_offsets, self.w13, self.w2,
-                          self.yp, self.ffn_ws, self.status, stream)
+                          self.yp, self.ffn_ws, self.status, stream,
+                          max_ctas=self.ffn_ctas)
 
     def combine(self, topk_gate=None, y=None, stream=None):
         gate = self.topk_gate if topk_gate is None else topk_gate
@@ -352,6 +359,77 @@ class MoELayer:
         s.wait_stream(d2h)
         return ys_host
 
+    def twin(self):
+        """A second layer over the same weights with its own device
+        buffers (routing, layout, expert rows, workspaces, output)."""
+        a = self._init_args
+        return MoELayer(a["T"], a["D"], a["E"], a["k"], a["R"], self.w_r,
+                        self.w13, self.w2, F=a["F"], score=a["score"],
+                        sel_bias=self.sel_bias,
+                        logit_offset=self.logit_offset,
+                        capacity_factor=a["capacity_factor"],
+                        n_groups=a["n_groups"], topk_groups=a["topk_groups"],
+                        group_score_topk=a["group_score_topk"],
+                        device=self.device, keep_logits=a["keep_logits"])
+
+    def forward_overlapped(self, xs, ys, stream=None, ffn_ctas=None):
+        """Micro-batches xs[i] -> ys[i] (each [T, D] on the device, each its
+        own routing decision and capacity), with the routing, layout and
+        permute of batch i+1 on a second stream while the grouped FFN and
+        combine of batch i run ("Expert Parallelism in LLMs", Overlapping
+        All-to-All with Computation: the dispatch of one micro-batch runs
+        while another computes).  The grouped FFN runs on ffn_ctas CTAs
+        (default: all SMs but 8) so that SMs stay free for the other
+        stream.  Two buffer sets alternate (this layer and its twin).
+        Returns ys; each ys[i] equals forward(xs[i]) bit for bit."""
+        if self.padded:
+            raise ValueError("overlap runs the compact layout")
+        s = stream or torch.cuda.current_stream()
+        if getattr(self, "_overlap", None) is None:
+            self._overlap = dict(twin=self.twin(),
+                                 side=torch.cuda.Stream(device=self.device))
+        o = self._overlap
+        layers = [self, o["twin"]]
+        side = o["side"]
+        if ffn_ctas is None:
+            n_sms = torch.cuda.get_device_properties(
+                self.device).multi_processor_count
+            ffn_ctas = max(2, n_sms - 8)
+        n = len(xs)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        front_done = [ev() for _ in range(n)]
+        back_done = [ev() for _ in range(n)]
+        side.wait_stream(s)
+
+        def front(i):
+            lay = layers[i % 2]
+            with torch.cuda.stream(side):
+                if i >= 2:
+                    side.wait_event(back_done[i - 2])
+                lay.route(xs[i], side)
+                lay.dispatch_layout(None, side)
+                lay.permute(xs[i], side)
+                front_done[i].record(side)
+
+        saved = [lay.ffn_ctas for lay in layers]
+        for lay in layers:
+            lay.ffn_ctas = ffn_ctas
+        try:
+            front(0)
+            for i in range(n):
+                if i + 1 < n:
+                    front(i + 1)
+                lay = layers[i % 2]
+                s.wait_event(front_done[i])
+                lay.grouped_ffn(s)
+                lay.combine(None, ys[i], s)
+                back_done[i].record(s)
+        finally:
+            for lay, c in zip(layers, saved):
+                lay.ffn_ctas = c
+        s.wait_stream(side)
+        return ys
+
     def capture(self, x, topk_idx=None, topk_gate=None, train=False):
         """Captures one forward pass on the device input buffer `x` (its
         storage is reused at every replay) into a CUDA graph and returns a
@@ -392,4 +470,8 @@ class MoELayer:
         return replay
 
     def device_status(self) -> int:
-        return int(self.status.item())
+        st = int(self.status.item())
+        o = getattr(self, "_overlap", None)
+        if st == 0 and o is not None:
+            st = int(o["twin"].status.item())
+        return st

@@ -313,6 +313,33 @@ def test_route_group_ties_go_to_lower_index(groups):
     assert np.abs(gate - rgate).max() <= 2e-6
 
 
+@pytest.mark.parametrize("E,groups,k", [(256, (8, 4, 2), 8), (64, (1, 1, 0), 6),
+                                         (32, (4, 2, 3), 4), (256, (8, 3, 8), 8)])
+def test_sigmoid_route_near_ties(E, groups, k):
+    # sigmoid keys that differ by a few fp32 ulp (logits on a fine grid, bias
+    # steps of 2^-23): the approximate keys cannot order these experts, so
+    # most of them must go through the exact evaluation (several rounds of
+    # 32); ids must still equal the oracle's definitional selection, bit for
+    # bit, on the logits the kernel used
+    T, D = 96, 64
+    g = torch.Generator().manual_seed(E + k)
+    # x . w = one-hot rows of w pick logits from a fine grid around 0.3
+    x = torch.zeros((T, D))
+    x[:, 0] = 1.0
+    w = torch.zeros((E, D))
+    w[:, 0] = 0.3 + torch.randint(-40, 40, (E,), generator=g).float() * 2.0 ** -22
+    for t in range(T):
+        x[t, 1 + t % (D - 1)] = 2.0 ** -20 * (t % 7)
+    w[:, 1:] = torch.randint(-3, 4, (E, D - 1), generator=g).float()
+    b = torch.randint(-4, 5, (E,), generator=g).float() * 2.0 ** -23
+    idx, gate, logits = run_route(x.float(), w.float(), None, b, k,
+                                  "sigmoid_bias", groups)
+    ridx, rgate = O.route_from_logits(logits, k, "sigmoid_bias", b.numpy(),
+                                      *groups)
+    assert (idx == ridx).all()
+    assert np.abs(gate - rgate).max() <= 2e-6
+
+
 def test_sigmoid_key_bit_exact():
     # the selection score is an integer decision's input: the device's
     # fp32(sigmoid(l)) must equal the oracle's float64 sigmoid rounded once
@@ -637,6 +664,32 @@ def test_layer_parity_small(wl):
     ref = check_layer_vs_oracle(wl, inp, layer, y)
     if wl.capacity_factor is not None:
         assert int(layer.n_dropped.item()) == ref["dropped"]
+
+
+@pytest.mark.parametrize("wl", [
+    W.WORKLOADS["mixtral_bf16"].with_(T=512, D=1024, F=1024),
+    W.WORKLOADS["switch_bf16"].with_(T=2048, D=256, F=512),
+    W.WORKLOADS["deepseek_bf16"].with_(T=256, D=1024, E=64, F=256)],
+    ids=lambda w: w.name)
+def test_forward_overlapped_matches_forward(wl):
+    # micro-batches with the routing of batch i+1 on a second stream while
+    # batch i's experts run on fewer CTAs: every batch's output equals the
+    # plain forward pass of that batch, bit for bit (each batch keeps its own
+    # routing decision and capacity)
+    inp = W.make_inputs(wl, device="cpu")
+    layer = layer_from(wl, inp)
+    g = torch.Generator().manual_seed(77)
+    xs = [(torch.randn((wl.T, wl.D), generator=g)).to(inp["x"].dtype).to(DEV)
+          for _ in range(5)]
+    ref = []
+    for x in xs:
+        ref.append(layer.forward(x).clone())
+    ys = [torch.full_like(xs[0], float("nan")) for _ in xs]
+    layer.forward_overlapped(xs, ys, ffn_ctas=64)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    for a, b in zip(ys, ref):
+        assert torch.equal(a, b)
 
 
 def test_layer_repeatable_bitwise():
