@@ -97,3 +97,28 @@ def test_traffic_keys_match_workload_shapes(bench):
         # of 64 experts active) and below 1.2x
         m = bench.kernel_models(wl, wl.T * wl.k, 2, PEAKS)
         assert 0.25 * m["ffn"]["bytes"] < v < 1.2 * m["ffn"]["bytes"], name
+
+
+def test_bf16_peak_follows_the_run_regime(bench):
+    # the tensor denominator: burst when the timed region is short or the
+    # clocks never showed the power cap; sustained for a long capped run
+    peaks = {"bf16_tflops": 1775.0, "bf16_tflops_sustained": 1400.0,
+             "source": "measured"}
+    capped = {"reasons": ["sw_power_cap"]}
+    free = {"reasons": []}
+    assert bench.choose_bf16_peak(peaks, 0.03, capped)[0] == 1775.0
+    assert bench.choose_bf16_peak(peaks, 5.0, free)[0] == 1775.0
+    assert bench.choose_bf16_peak(peaks, 5.0, None)[0] == 1775.0
+    pk, note = bench.choose_bf16_peak(peaks, 5.0, capped)
+    assert pk == 1400.0 and "sustained" in note
+    assert "burst" in bench.choose_bf16_peak(peaks, 0.5, capped)[1]
+
+
+def test_default_run_measures_every_configuration(bench):
+    # the default line carries a sub-record for each configuration besides
+    # the headline, and every name is a known workload
+    names = set(bench.SUB_WORKLOADS)
+    assert names == {"deepseek_bf16", "switch_bf16", "tiny_f32",
+                     "sweep_bf16_uniform_T65536", "sweep_bf16_zipf_T65536"}
+    for n in names:
+        assert n in W.WORKLOADS
