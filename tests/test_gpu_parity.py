@@ -449,6 +449,12 @@ FFN_CASES = [
     # swapped and normal
     (4, 512, 2048, [300, 40, 0, 129], torch.bfloat16),
     (1, 256, 1024, [1000], torch.bfloat16),
+    # short tails (1..49 rows) after one or more full row blocks of the same
+    # expert, next to other experts' rows and, for the last expert, next to
+    # the unused rows at the end of the allocation
+    (7, 256, 256, [128 + 47, 256 + 48, 128 + 49, 384 + 16, 128 + 33, 0,
+                   128 + 1], torch.bfloat16),
+    (3, 320, 384, [256 + 32, 48, 128 + 48], torch.bfloat16),
 ]
 
 
