@@ -269,6 +269,13 @@ ROUTE_CASES = [
     # more row blocks than SMs, unevenly: the GEMM runs as two K halves
     (20000, 512, 64, 4, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
     (10000, 128, 64, 4, torch.bfloat16, "softmax_topk", (4, 2, 2), None, None, None),
+    # one-kernel router over more than one block per SM (T above 8 warps per
+    # SM), odd T: 8, 16 and 32 expert rows, bf16 and fp32, every score mode
+    (2049, 4096, 8, 2, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
+    (1999, 256, 32, 4, torch.bfloat16, "softmax_full", (1, 1, 0), None, 1.5, None),
+    (3001, 520, 12, 3, torch.bfloat16, "sigmoid_bias", (4, 2, 2), None, None, 0.1),
+    (1501, 96, 24, 5, torch.float32, "sigmoid_bias", (3, 2, 2), None, None, 0.05),
+    (1301, 64, 16, 4, torch.float32, "softmax_topk", (1, 1, 0), 0.02, None, None),
 ]
 
 
@@ -279,6 +286,22 @@ def test_route_parity(case):
                                      offset=offset, bias=bias)
     idx, gate, logits = run_route(x, w, off, b, k, score, groups)
     check_route(x, w, off, b, k, score, groups, idx, gate, logits)
+
+
+@pytest.mark.parametrize("E,D,dt", [(8, 4096, torch.bfloat16),
+                                    (32, 256, torch.bfloat16),
+                                    (16, 64, torch.float32)])
+def test_route_logits_independent_of_batch_size(E, D, dt):
+    # a token's logits are formed by its own warp in a fixed order, so they
+    # are the same bits whatever the call's T (one block or many per SM) and
+    # wherever the token sits in the batch
+    T = 4001
+    x, w, _, _ = make_route_inputs(T, D, E, dt, seed=E + D)
+    _, _, big = run_route(x, w, None, None, 2, "softmax_topk")
+    _, _, small = run_route(x[:100], w, None, None, 2, "softmax_topk")
+    assert np.array_equal(big[:100].view(np.int32), small.view(np.int32))
+    _, _, tail = run_route(x[-37:], w, None, None, 2, "softmax_topk")
+    assert np.array_equal(big[-37:].view(np.int32), tail.view(np.int32))
 
 
 @pytest.mark.parametrize("T", [512, 10240])
