@@ -132,14 +132,14 @@ def choose_bf16_peak(peaks, wall_s, clk):
 K_graph_cap = 200
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from ncu, keyed by
-# (workload, T, E, step), for the grouped FFN's one launch (up and down
-# projection) of the current kernel:
-#   Mixtral-like   3.0816 GB read + 145.4 MB written
-#   DeepSeek-like 23.3931 GB read + 598.7 MB written
-#   Switch-like    522.6 MB read +  17.4 MB written
-NCU_DRAM_BYTES = {("mixtral_bf16", 2048, 8, "ffn"): 3.2270e9,
-                  ("deepseek_bf16", 4096, 256, "ffn"): 2.39918e10,
-                  ("switch_bf16", 16384, 64, "ffn"): 5.400e8}
+# (workload, T, E, step, FFN variant as moe_grouped_ffn_variant reports it),
+# for the grouped FFN's one launch (up and down projection):
+#   Mixtral-like   3.5955 GB read + 187.4 MB written (SM pairs)
+#   DeepSeek-like 23.3931 GB read + 598.7 MB written (one SM per tile)
+#   Switch-like    522.6 MB read +  17.4 MB written (one SM per tile)
+NCU_DRAM_BYTES = {("mixtral_bf16", 2048, 8, "ffn", 3): 3.7829e9,
+                  ("deepseek_bf16", 4096, 256, "ffn", 2): 2.39918e10,
+                  ("switch_bf16", 16384, 64, "ffn", 2): 5.400e8}
 
 # tokens of the bounded CPU-oracle sample, per workload (about 10-30 s of
 # host work)
@@ -299,13 +299,22 @@ SUB_WORKLOADS = ("deepseek_bf16", "switch_bf16", "tiny_f32",
 STAGES = ["route", "layout", "permute", "ffn", "combine"]
 
 
+def ffn_variant(layer):
+    from combine_router_gemm_top_b300 import _lib as L
+    return L.moe_grouped_ffn_variant(layer.E, layer.D, layer.F,
+                                     layer.T * layer.k, layer.dcode)
+
+
 def kernel_label(layer, key):
     from combine_router_gemm_top_b300 import _lib as L
     n_layout = L.moe_dispatch_layout_launches(layer.T, layer.k, layer.E)
     return {
-        "ffn": ("moe_grouped_ffn (one tcgen05 launch, up + down)"
-                if layer.dcode == L.MOE_BF16 else
-                "moe_grouped_ffn (fp32: up and down kernels on CUDA cores)"),
+        "ffn": {1: "moe_grouped_ffn (fp32: up and down kernels on CUDA cores)",
+                2: "moe_grouped_ffn (one tcgen05 launch, up + down, one SM "
+                   "per 128-row tile)",
+                3: "moe_grouped_ffn (one tcgen05 launch, up + down, SM pairs "
+                   "on 256-row tiles)"}.get(ffn_variant(layer),
+                                            "moe_grouped_ffn"),
         "route": ("moe_route (one warp-per-token kernel)"
                   if L.moe_route_launches(layer.cfg) == 1 else
                   "moe_route (router GEMM + select)"),
@@ -397,7 +406,7 @@ def measure(args, wl, dev, rank, world, local_rank, dist):
     # DRAM bytes (read + write) of one launch of the dominant kernel, from an
     # ncu capture of the same kernel on the same workload; re-take it when
     # the kernel changes.
-    dram = NCU_DRAM_BYTES.get((wl.name, wl.T, wl.E, dom))
+    dram = NCU_DRAM_BYTES.get((wl.name, wl.T, wl.E, dom, ffn_variant(layer)))
     if dram is not None:
         roof["traffic"] = dram
         roof["traffic_over_algorithmic"] = round(dram / dm["bytes"], 3)

@@ -37,6 +37,7 @@ EXPORTED = ["moe_route_workspace_size", "moe_route_launches", "moe_route",
             "moe_dispatch_layout_workspace_size",
             "moe_dispatch_layout_launches", "moe_dispatch_layout",
             "moe_permute", "moe_grouped_ffn_workspace_size",
+            "moe_grouped_ffn_variant",
             "moe_grouped_ffn", "moe_combine", "moe_selftest_bounded_wait",
             "moe_selftest_sigmoid_key", "moe_dispatch_layout_noalloc",
             "moe_router_stats_workspace_size", "moe_router_stats",
@@ -85,6 +86,7 @@ _SIGS = {
     "moe_permute": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _i32, _vp,
                            _vp]),
     "moe_grouped_ffn_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "moe_grouped_ffn_variant": (_i32, [_i32, _i32, _i32, _i32, _i32]),
     "moe_grouped_ffn": (_i32, [_i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp,
                                _vp, _vp, _vp, _sz, _i32, _vp, _vp]),
     "moe_combine": (_i32, [_i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _i32,
@@ -254,6 +256,10 @@ def moe_permute(T, k, D, dtype, x, dst_row, xp, status=None, stream=None,
 
 def moe_grouped_ffn_workspace_size(E, D, F, max_rows, dtype) -> int:
     return load().moe_grouped_ffn_workspace_size(E, D, F, max_rows, dtype)
+
+
+def moe_grouped_ffn_variant(E, D, F, max_rows, dtype) -> int:
+    return load().moe_grouped_ffn_variant(E, D, F, max_rows, dtype)
 
 
 def moe_grouped_ffn(E, D, F, max_rows, dtype, xp, expert_offsets, w13, w2,

@@ -235,6 +235,28 @@ size_t moe_grouped_ffn_workspace_size(int32_t E, int32_t D, int32_t F,
   return b > 0 ? b : 16;
 }
 
+// Shape and dtype checks of moe_grouped_ffn (pointers aside).
+static moe_status ffn_shape_status(int32_t E, int32_t D, int32_t F,
+                                   int32_t max_rows, int32_t dtype) {
+  if (E < 1 || D <= 0 || F <= 0 || max_rows < 0 || !valid_dtype(dtype))
+    return MOE_ERR_INVALID;
+  if (dtype == MOE_BF16) {
+    if (D % 64 != 0 || F % 128 != 0 || E > kMaxGroupsApi)
+      return MOE_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(E) * 2 * F > INT32_MAX ||
+        static_cast<int64_t>(E) * D > INT32_MAX)
+      return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+int32_t moe_grouped_ffn_variant(int32_t E, int32_t D, int32_t F,
+                                int32_t max_rows, int32_t dtype) {
+  if (ffn_shape_status(E, D, F, max_rows, dtype) != MOE_OK || max_rows == 0)
+    return 0;
+  return ffn_variant(E, F, max_rows, dtype);
+}
+
 moe_status moe_grouped_ffn(int32_t E, int32_t D, int32_t F, int32_t max_rows,
                            int32_t dtype, const void* xp,
                            const int32_t* expert_offsets, const void* w13,
@@ -249,12 +271,9 @@ moe_status moe_grouped_ffn(int32_t E, int32_t D, int32_t F, int32_t max_rows,
     return MOE_ERR_INVALID;
   if (workspace_bytes < ffn_ws_bytes(E, D, F, max_rows, dtype))
     return MOE_ERR_INVALID;
+  const moe_status shape = ffn_shape_status(E, D, F, max_rows, dtype);
+  if (shape != MOE_OK) return shape;
   if (dtype == MOE_BF16) {
-    if (D % 64 != 0 || F % 128 != 0 || E > kMaxGroupsApi)
-      return MOE_ERR_UNSUPPORTED;
-    if (static_cast<int64_t>(E) * 2 * F > INT32_MAX ||
-        static_cast<int64_t>(E) * D > INT32_MAX)
-      return MOE_ERR_UNSUPPORTED;
     if (!aligned(xp, 256) || !aligned(w13, 256) || !aligned(w2, 256) ||
         !aligned(yp, 16) || !aligned(workspace, 256))
       return MOE_ERR_INVALID;

@@ -17,6 +17,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "umma_ffn.cuh"
+#include "umma_ffn_pair.cuh"
 #include "umma_gemm.cuh"
 
 namespace moe {
@@ -73,7 +74,8 @@ __global__ void ffn_down_f32_kernel(int E, int D, int F, int max_rows,
 
 // ----------------------------------------------------------- host
 // Workspace: H [max_rows, F], then (bf16) one ready counter per row block of
-// the fused launch: at most ceil(max_rows / 128) + E blocks.
+// the fused launch (at most ceil(max_rows / 128) + E blocks) and the SM-pair
+// launch's tile ticket.
 static size_t ffn_h_bytes(int F, int max_rows, int dtype) {
   return (static_cast<size_t>(max_rows) * F * dtype_bytes(dtype) + 255) &
          ~size_t(255);
@@ -87,7 +89,89 @@ size_t ffn_ws_bytes(int E, int D, int F, int max_rows, int dtype) {
   if (dtype != MOE_BF16)
     return static_cast<size_t>(max_rows) * F * dtype_bytes(dtype);
   return ffn_h_bytes(F, max_rows, dtype) +
-         static_cast<size_t>(ffn_ready_cap(E, max_rows)) * sizeof(uint32_t);
+         static_cast<size_t>(ffn_ready_cap(E, max_rows) + 1) * sizeof(uint32_t);
+}
+
+int ffn_variant(int E, int F, int max_rows, int dtype) {
+  if (dtype == MOE_F32) return 1;
+  // SM pairs when the experts average at least 1.5 pair row blocks (256
+  // rows): below that the 256-row blocks waste more rows than the pairs
+  // save
+  return F % 256 == 0 && E <= kPairMaxGroups &&
+                 static_cast<int64_t>(max_rows) >= 384LL * E
+             ? 3
+             : 2;
+}
+
+// SM pairs (umma_ffn_pair.cuh): persistent 2-CTA clusters, at most as many
+// as fit at once (more would only find the tile ticket used up).  Tiles are
+// claimed in order, so no cluster waits on one that is not running and the
+// launch needs no co-residency guarantee.
+static moe_status launch_ffn_pair(int E, int D, int F, int max_rows,
+                                  const void* xp, const int32_t* offsets,
+                                  const void* w13, const void* w2, void* yp,
+                                  void* h, uint32_t* ready, int ready_cap,
+                                  int max_ctas, int32_t* status,
+                                  cudaStream_t stream, int num_sms) {
+  CUtensorMap tm_xp, tm_w13, tm_h, tm_w2, tm_xp_t, tm_h_t;
+  if (!make_tmap_bf16_2d(&tm_xp, xp, D, max_rows, 128) ||
+      !make_tmap_bf16_2d(&tm_w13, w13, D, static_cast<int64_t>(E) * 2 * F, 128) ||
+      !make_tmap_bf16_2d(&tm_h, h, F, max_rows, 128) ||
+      !make_tmap_bf16_2d(&tm_w2, w2, F, static_cast<int64_t>(E) * D, 128) ||
+      !make_tmap_bf16_2d(&tm_xp_t, xp, D, max_rows, kPairSwapMax / 2) ||
+      !make_tmap_bf16_2d(&tm_h_t, h, F, max_rows, kPairSwapMax / 2))
+    return MOE_ERR_CUDA;
+  PairFfnArgs a{};
+  a.E = E;
+  a.D = D;
+  a.F = F;
+  a.kb_up = D / kBK;
+  a.kb_dn = F / kBK;
+  a.n_up = F / 128;
+  a.S = F / 256;
+  a.n_dn = static_cast<int>(ceil_div(D, 256));
+  a.offsets = offsets;
+  a.max_rows = max_rows;
+  a.h = static_cast<__nv_bfloat16*>(h);
+  a.yp = static_cast<__nv_bfloat16*>(yp);
+  a.ready = ready;
+  a.ready_cap = ready_cap;
+  a.ticket = ready + ready_cap;
+  a.status = status;
+  a.wait_limit_ns = kWaitLimitNs;
+  static std::atomic<uint64_t> attr_done{0};
+  if (!set_smem_limit_once(reinterpret_cast<const void*>(umma_ffn_pair_kernel),
+                           227 * 1024, &attr_done))
+    return MOE_ERR_CUDA;
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = umma_ffn_pair_smem_bytes();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms / 2 * 2));
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, umma_ffn_pair_kernel, &cfg) !=
+          cudaSuccess ||
+      clusters < 1) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  int want = max_ctas > 0 && max_ctas < num_sms ? max_ctas / 2 : num_sms / 2;
+  if (want < 1) want = 1;
+  cfg.gridDim =
+      dim3(static_cast<unsigned>(2 * (want < clusters ? want : clusters)));
+  if (cudaLaunchKernelEx(&cfg, umma_ffn_pair_kernel, tm_xp, tm_w13, tm_h,
+                         tm_w2, tm_xp_t, tm_h_t, a) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
 
@@ -152,10 +236,14 @@ moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
   f.ready = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) +
                                         ffn_h_bytes(F, max_rows, dtype));
   f.ready_cap = ffn_ready_cap(E, max_rows);
-  if (cudaMemsetAsync(f.ready, 0, static_cast<size_t>(f.ready_cap) *
+  if (cudaMemsetAsync(f.ready, 0, static_cast<size_t>(f.ready_cap + 1) *
                                       sizeof(uint32_t),
                       stream) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (ffn_variant(E, F, max_rows, dtype) == 3)
+    return launch_ffn_pair(E, D, F, max_rows, xp, offsets, w13, w2, yp, h,
+                           f.ready, f.ready_cap, max_ctas, status, stream,
+                           num_sms);
   static std::atomic<uint64_t> attr_done{0};
   if (!set_smem_limit_once(reinterpret_cast<const void*>(umma_ffn_kernel),
                            227 * 1024, &attr_done))

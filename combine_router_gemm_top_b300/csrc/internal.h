@@ -70,6 +70,8 @@ moe_status launch_combine(int T, int k, int D, int dtype, const void* yp,
                           int num_sms);
 
 size_t ffn_ws_bytes(int E, int D, int F, int max_rows, int dtype);
+// moe_grouped_ffn_variant's answer for valid arguments (1, 2 or 3).
+int ffn_variant(int E, int F, int max_rows, int dtype);
 moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
                               const void* xp, const int32_t* offsets,
                               const void* w13, const void* w2, void* yp,

@@ -297,6 +297,12 @@ __device__ __forceinline__ void cluster_sync_all() {
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// 32-bit store to a shared::cluster address (another CTA of the cluster).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr,
+                                               uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v)
+               : "memory");
+}
 // Arrive once on an mbarrier of another CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"

@@ -235,10 +235,21 @@ MOE_API moe_status moe_permute(int32_t T, int32_t k, int32_t D, int32_t dtype,
 
 /* Bytes of scratch moe_grouped_ffn needs: the SwiGLU hidden activations
  * H [max_rows, F] in the compute dtype, then (bf16) one 32-bit counter per
- * 128-row block (ceil(max_rows / 128) + E), which the call zeroes itself on
- * the stream. */
+ * 128-row block (ceil(max_rows / 128) + E) and one tile ticket, which the
+ * call zeroes itself on the stream. */
 MOE_API size_t moe_grouped_ffn_workspace_size(int32_t E, int32_t D, int32_t F,
                                       int32_t max_rows, int32_t dtype);
+
+/* moe_grouped_ffn_variant -- which implementation moe_grouped_ffn runs for
+ * this size: 1 = fp32 FMA kernels (MOE_F32, two launches); 2 = one
+ * persistent tcgen05 launch with a 128-row tile on each SM (cooperative);
+ * 3 = one persistent tcgen05 launch of SM pairs (2-CTA clusters,
+ * cta_group::2) with 256-row tiles claimed in order, taken when the experts
+ * average at least 384 rows (max_rows >= 384 E), F % 256 == 0 and
+ * E <= 256; 0 for arguments moe_grouped_ffn rejects or max_rows = 0.
+ * Host only. */
+MOE_API int32_t moe_grouped_ffn_variant(int32_t E, int32_t D, int32_t F,
+                                        int32_t max_rows, int32_t dtype);
 
 /* moe_grouped_ffn -- per-expert SwiGLU over ragged expert segments
  * ("Expert Parallelism in LLMs", The Execution Pipeline, step 4 "Local
@@ -261,10 +272,13 @@ MOE_API size_t moe_grouped_ffn_workspace_size(int32_t E, int32_t D, int32_t F,
  * needs D % 64 == 0 and F % 128 == 0 (else MOE_ERR_UNSUPPORTED).  It is one
  * persistent launch for both projections in which tiles of the down
  * projection wait (bounded) for the up-projection tiles of their rows held
- * by other CTAs; the launch is cooperative, so CUDA makes every CTA
- * resident at once, and a device that cannot host the grid fails the call
- * with MOE_ERR_CUDA instead of stalling.  MOE_F32 runs fp32 FMA (max_ctas
- * unused). */
+ * by other CTAs.  With one SM per tile the CTAs walk a fixed schedule, so
+ * the launch is cooperative: CUDA makes every CTA resident at once, and a
+ * device that cannot host the grid fails the call with MOE_ERR_CUDA instead
+ * of stalling.  Experts with many rows run on SM pairs instead
+ * (moe_grouped_ffn_variant), which claim tiles in order and need no
+ * co-residency; max_ctas is then rounded down to whole pairs.  MOE_F32 runs
+ * fp32 FMA (max_ctas unused). */
 MOE_API moe_status moe_grouped_ffn(int32_t E, int32_t D, int32_t F, int32_t max_rows,
                            int32_t dtype, const void* xp,
                            const int32_t* expert_offsets, const void* w13,

@@ -133,6 +133,27 @@ def test_layout_launches(lib):
     assert lib.moe_dispatch_layout_launches(16, 2, 2000) == 0
 
 
+def test_grouped_ffn_variant(lib):
+    # 1: fp32 FMA; 2: one SM per 128-row tile; 3: SM pairs, taken for
+    # F % 256 == 0, E <= 256 and max_rows >= 384 E; 0: rejected or empty
+    bf, f32 = L.MOE_BF16, L.MOE_F32
+    for args, v in [((8, 4096, 14336, 4096, bf), 3),     # Mixtral-like
+                    ((8, 4096, 14336, 3071, bf), 2),
+                    ((8, 4096, 14336, 3072, bf), 3),
+                    ((8, 4096, 14208, 8192, bf), 2),     # F % 256 = 128
+                    ((256, 7168, 2048, 32768, bf), 2),   # DeepSeek-like
+                    ((256, 7168, 2048, 98304, bf), 3),
+                    ((256, 256, 256, 384 * 256, bf), 3),
+                    ((256, 256, 256, 384 * 256 - 1, bf), 2),
+                    ((257, 256, 256, 1 << 20, bf), 2),   # E > 256
+                    ((64, 1024, 4096, 16384, bf), 2),    # Switch-like
+                    ((8, 64, 128, 4096, f32), 1),
+                    ((8, 4096, 14336, 0, bf), 0),
+                    ((8, 4000, 14336, 4096, bf), 0),     # D % 64 != 0
+                    ((0, 4096, 14336, 4096, bf), 0)]:
+        assert lib.moe_grouped_ffn_variant(*args) == v, args
+
+
 def test_permute_combine_reject(lib):
     R = 20   # rows of the expert-contiguous buffer
     assert lib.moe_permute(10, 2, 12, L.MOE_BF16, FAKE, FAKE, FAKE, R, None,
@@ -197,9 +218,10 @@ def test_grouped_ffn_reject(lib):
     assert lib.moe_grouped_ffn(8, 128, 256, 64, L.MOE_BF16, FAKE, None, FAKE,
                                FAKE, FAKE, FAKE, ok_ws, 0, None, None) == \
         L.MOE_ERR_INVALID
-    # H [max_rows, F], then one counter per row block (ceil(64/128) + E)
+    # H [max_rows, F], then one counter per row block (ceil(64/128) + E) and
+    # the SM-pair launch's tile ticket
     assert lib.moe_grouped_ffn_workspace_size(8, 128, 256, 64, L.MOE_BF16) == \
-        64 * 256 * 2 + (1 + 8) * 4
+        64 * 256 * 2 + (1 + 8 + 1) * 4
     assert lib.moe_grouped_ffn_workspace_size(8, 128, 256, 64, L.MOE_F32) == \
         64 * 256 * 4
 

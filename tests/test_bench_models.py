@@ -86,17 +86,24 @@ def test_route_work_and_bound(bench):
 
 
 def test_traffic_keys_match_workload_shapes(bench):
-    # each ncu traffic figure is looked up by (workload, T, E, step); a key
-    # whose shape differs from the workload's would never be found
-    for (name, T, E, step), v in bench.NCU_DRAM_BYTES.items():
+    # each ncu traffic figure is looked up by (workload, T, E, step, FFN
+    # variant); a key whose shape or kernel differs from the workload's
+    # would never be found
+    from combine_router_gemm_top_b300 import _lib as L
+    from combine_router_gemm_top_b300 import build as B
+    B.build(verbose=False)
+    for (name, T, E, step, variant), v in bench.NCU_DRAM_BYTES.items():
         wl = W.WORKLOADS[name]
         assert (wl.T, wl.E) == (T, E), name
         assert step == "ffn" and not wl.identity_experts
+        assert L.moe_grouped_ffn_variant(wl.E, wl.D, wl.F, wl.T * wl.k,
+                                         L.MOE_BF16) == variant, name
         # a figure of the right order against all experts' weights plus
         # activations: above a quarter of them (the Switch-like layer has 20
-        # of 64 experts active) and below 1.2x
+        # of 64 experts active) and below 1.5x (the SM-pair kernel's swapped
+        # tail tiles re-read their weight tiles: 1.31x measured)
         m = bench.kernel_models(wl, wl.T * wl.k, 2, PEAKS)
-        assert 0.25 * m["ffn"]["bytes"] < v < 1.2 * m["ffn"]["bytes"], name
+        assert 0.25 * m["ffn"]["bytes"] < v < 1.5 * m["ffn"]["bytes"], name
 
 
 def test_bf16_peak_follows_the_run_regime(bench):

@@ -499,6 +499,57 @@ def test_grouped_ffn_parity(case):
     assert torch.isnan(yp[n:].float()).all()
 
 
+PAIR_FFN_CASES = [
+    # E, D, F, counts: experts averaging >= 384 rows run on SM pairs with
+    # 256-row blocks.  Tails of 1..64 rows run swapped; longer remainders
+    # are a block whose rows past the expert's are computed, not stored.
+    (2, 256, 512, [256 + 1, 512 + 64]),
+    (3, 320, 256, [256 + 65, 128, 512 + 16]),      # D = 320: half-outside
+    (4, 256, 256, [40, 0, 700, 256 + 44]),         # a tail-only expert
+    (2, 512, 512, [512, 256]),                     # full blocks only
+    (1, 256, 1024, [1000]),                        # 16 K blocks down
+    (8, 1024, 512, [100, 300, 0, 17, 128, 129, 255, 1]),
+]
+
+
+def pair_ffn_inputs(E, D, F, counts, seed):
+    n = sum(counts)
+    max_rows = max(n + 37, 384 * E)
+    assert L.moe_grouped_ffn_variant(E, D, F, max_rows,
+                                     L.dtype_code(torch.bfloat16)) == 3
+    g = torch.Generator().manual_seed(seed)
+    xp = torch.randn((max_rows, D), generator=g).to(torch.bfloat16)
+    std = 1.0 / math.sqrt(D)
+    w13 = (torch.randn((E, 2 * F, D), generator=g) * std).to(torch.bfloat16)
+    w2 = (torch.randn((E, D, F), generator=g) * std).to(torch.bfloat16)
+    return n, xp, w13, w2
+
+
+@pytest.mark.parametrize("case", PAIR_FFN_CASES)
+def test_grouped_ffn_pairs_parity(case):
+    E, D, F, counts = case
+    n, xp, w13, w2 = pair_ffn_inputs(E, D, F, counts, seed=E * 77 + D)
+    yp, off = run_ffn(xp, counts, w13, w2, F)
+    ref = O.grouped_ffn(f64(xp)[:n], off, f64(w13), f64(w2))
+    got = f64(yp[:n])
+    assert np.isfinite(got).all()
+    assert rel_err(got, ref) <= tol_for(torch.bfloat16)
+    assert torch.isnan(yp[n:].float()).all()
+
+
+@pytest.mark.parametrize("ctas", [2, 8, 37])
+def test_grouped_ffn_pairs_on_few_ctas(ctas):
+    # the pair launch on a grid of a few clusters (an odd request rounds
+    # down to whole pairs): same bits as on every SM
+    E, D, F, counts = 3, 512, 512, [600, 40, 513]
+    n, xp, w13, w2 = pair_ffn_inputs(E, D, F, counts, seed=93)
+    yp, off = run_ffn(xp, counts, w13, w2, F, max_ctas=ctas)
+    ref = O.grouped_ffn(f64(xp)[:n], off, f64(w13), f64(w2))
+    assert rel_err(f64(yp[:n]), ref) <= 1e-2
+    full, _ = run_ffn(xp, counts, w13, w2, F)
+    assert torch.equal(yp[:n], full[:n])
+
+
 @pytest.mark.parametrize("ctas", [1, 8, 37])
 def test_grouped_ffn_on_few_ctas(ctas):
     # the persistent launch on a grid far below the SM count: every CTA walks
