@@ -509,6 +509,9 @@ PAIR_FFN_CASES = [
     (2, 512, 512, [512, 256]),                     # full blocks only
     (1, 256, 1024, [1000]),                        # 16 K blocks down
     (8, 1024, 512, [100, 300, 0, 17, 128, 129, 255, 1]),
+    (1, 64, 256, [400]),                           # one K block up
+    (16, 128, 256, [300, 511, 512, 513, 320, 257, 575, 576, 577, 0, 64,
+                    700, 310, 450, 290, 333]),
 ]
 
 
