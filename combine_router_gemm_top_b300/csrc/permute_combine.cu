@@ -125,6 +125,75 @@ __global__ void __launch_bounds__(kRowWarps * 32)
   }
 }
 
+// k = 2: both slots' row vectors are loaded before any arithmetic, so a
+// step costs one memory round trip instead of two; each vector is then
+// reduced and stored on its own, so only its 8 (bf16) accumulators are live
+// and the block fits 4 times per SM.  The fp32 operations and their
+// order are combine_kernel's: y = fma(g1, x1, fma(g0, x0, 0)), a dropped slot
+// skipped.
+template <typename T, bool SEG>
+__global__ void __launch_bounds__(kRowWarps * 32, 4)
+    combine2_kernel(int64_t n_tok, int nvec, int nseg_arg,
+                    const uint4* __restrict__ yp,
+                    const int32_t* __restrict__ dst_row,
+                    const float* __restrict__ gate, uint4* __restrict__ y,
+                    int max_rows, int32_t* status) {
+  constexpr int N = Vec16<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_g = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kRowWarps;
+  const int nseg = SEG ? nseg_arg : 1;
+  const int segv = nvec / nseg;
+  for (int64_t u = warp_g; u < n_tok * nseg; u += nwarps) {
+    const int64_t t = u / nseg;
+    const int v_begin = static_cast<int>(u - t * nseg) * segv;
+    const int v_end = v_begin + segv;
+    const int32_t my_dst = checked_row(
+        lane < 2 ? __ldg(dst_row + t * 2 + lane) : -1, max_rows, status);
+    const float my_g =
+        lane < 2 ? (gate != nullptr ? __ldg(gate + t * 2 + lane) : 1.0f)
+                 : 0.0f;
+    const int32_t r0 = __shfl_sync(0xffffffffu, my_dst, 0);
+    const int32_t r1 = __shfl_sync(0xffffffffu, my_dst, 1);
+    const float g0 = __shfl_sync(0xffffffffu, my_g, 0);
+    const float g1 = __shfl_sync(0xffffffffu, my_g, 1);
+    const uint4* s0 = yp + static_cast<int64_t>(r0 < 0 ? 0 : r0) * nvec;
+    const uint4* s1 = yp + static_cast<int64_t>(r1 < 0 ? 0 : r1) * nvec;
+    uint4* out = y + t * nvec;
+    for (int v0 = v_begin + lane; v0 < v_end; v0 += 32 * kUnroll) {
+      uint4 b0[kUnroll], b1[kUnroll];
+#pragma unroll
+      for (int w = 0; w < kUnroll; ++w) {
+        const int v = v0 + w * 32;
+        const bool in = v < v_end;
+        b0[w] = in && r0 >= 0 ? ld_nc_v4(s0 + v) : make_uint4(0u, 0u, 0u, 0u);
+        b1[w] = in && r1 >= 0 ? ld_nc_v4(s1 + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int w = 0; w < kUnroll; ++w) {
+        const int v = v0 + w * 32;
+        if (v >= v_end) continue;
+        float acc[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[i] = 0.0f;
+        if (r0 >= 0) {
+          float f[N];
+          Vec16<T>::to_f32(b0[w], f);
+#pragma unroll
+          for (int i = 0; i < N; ++i) acc[i] = fmaf(g0, f[i], acc[i]);
+        }
+        if (r1 >= 0) {
+          float f[N];
+          Vec16<T>::to_f32(b1[w], f);
+#pragma unroll
+          for (int i = 0; i < N; ++i) acc[i] = fmaf(g1, f[i], acc[i]);
+        }
+        st_v4(out + v, Vec16<T>::from_f32(acc));
+      }
+    }
+  }
+}
+
 // Segments per row: double while the warps would number fewer than 48 per
 // SM and each segment keeps at least 128 vectors (one full step of 32 lanes
 // x 4); a segment count always divides nvec.
@@ -173,6 +242,15 @@ moe_status launch_combine(int T, int k, int D, int dtype, const void* yp,
   const unsigned grid = row_grid(static_cast<int64_t>(T) * nseg, num_sms);
   const uint4* src = static_cast<const uint4*>(yp);
   uint4* dst = static_cast<uint4*>(y);
+  if (k == 2 && dtype == MOE_BF16) {
+    if (nseg > 1)
+      combine2_kernel<__nv_bfloat16, true><<<grid, kRowWarps * 32, 0, stream>>>(
+          T, nvec, nseg, src, dst_row, gate, dst, max_rows, status);
+    else
+      combine2_kernel<__nv_bfloat16, false><<<grid, kRowWarps * 32, 0, stream>>>(
+          T, nvec, 1, src, dst_row, gate, dst, max_rows, status);
+    return launch_status();
+  }
   if (dtype == MOE_BF16) {
     if (nseg > 1)
       combine_kernel<__nv_bfloat16, true><<<grid, kRowWarps * 32, 0, stream>>>(
