@@ -12,12 +12,12 @@
 //           traffic N*D*s read + T*D*s written.
 //
 // One warp per (token, row segment); each lane moves 16-byte vectors, up
-// to 4 in flight per step for memory-level parallelism.  Row ids at or past
+// to 4 in flight per step for memory-level parallelism (for a bf16 combine
+// with k = 2, 4 per slot, both slots in one round trip).  Row ids at or past
 // the buffer's max_rows are skipped (never read or written) and reported as
-// MOE_ERR_INDEX.  A row is one
-// segment unless there are too few tokens to keep HBM busy: then it is cut
-// into up to 4 segments of at least 128 vectors, each its own warp (for
-// combine only with k <= 4).
+// MOE_ERR_INDEX.  A row is one segment unless there are too few tokens to
+// keep HBM busy: then it is cut into up to 4 segments of at least 128
+// vectors, each its own warp (for combine only with k <= 4).
 #include "common.cuh"
 #include "internal.h"
 
