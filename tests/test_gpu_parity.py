@@ -584,6 +584,48 @@ def test_grouped_ffn_all_experts_empty():
     assert torch.isnan(yp.float()).all()
 
 
+@pytest.mark.parametrize("E,max_rows,variant", [(2, 128, 2), (2, 768, 3)])
+def test_grouped_ffn_offsets_past_the_rows_run_nothing(E, max_rows, variant):
+    # offsets implying more row blocks than the workspace's counters cover
+    # (far past max_rows): both kernels report MOE_ERR_INVALID and run no
+    # tile, so yp keeps its sentinels
+    D, F = 128, 256
+    assert L.moe_grouped_ffn_variant(E, D, F, max_rows,
+                                     L.dtype_code(torch.bfloat16)) == variant
+    g = torch.Generator().manual_seed(7)
+    xp = torch.randn((max_rows, D), generator=g).to(torch.bfloat16).to(DEV)
+    w13 = (torch.randn((E, 2 * F, D), generator=g) * 0.05).to(
+        torch.bfloat16).to(DEV)
+    w2 = (torch.randn((E, D, F), generator=g) * 0.05).to(
+        torch.bfloat16).to(DEV)
+    off = torch.tensor([0, 3000, 6000][:E + 1], dtype=torch.int32, device=DEV)
+    yp = torch.full((max_rows, D), float("nan"), dtype=torch.bfloat16,
+                    device=DEV)
+    ws = torch.empty(L.moe_grouped_ffn_workspace_size(
+        E, D, F, max_rows, L.dtype_code(torch.bfloat16)), dtype=torch.uint8,
+        device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.moe_grouped_ffn(E, D, F, max_rows, L.dtype_code(torch.bfloat16), xp,
+                      off, w13, w2, yp, ws, st)
+    torch.cuda.synchronize()
+    assert st.item() == L.MOE_ERR_INVALID
+    assert torch.isnan(yp.float()).all()
+
+
+def test_grouped_ffn_pairs_all_experts_empty():
+    # the SM-pair kernel with every expert empty: the first claimed tile is
+    # past the end, every pair leaves, the output rows stay untouched
+    E, D, F, max_rows = 4, 128, 256, 1536
+    assert L.moe_grouped_ffn_variant(E, D, F, max_rows,
+                                     L.dtype_code(torch.bfloat16)) == 3
+    g = torch.Generator().manual_seed(6)
+    xp = torch.randn((max_rows, D), generator=g).to(torch.bfloat16)
+    w13 = (torch.randn((E, 2 * F, D), generator=g) * 0.05).to(torch.bfloat16)
+    w2 = (torch.randn((E, D, F), generator=g) * 0.05).to(torch.bfloat16)
+    yp, _ = run_ffn(xp, [0] * E, w13, w2, F)
+    assert torch.isnan(yp.float()).all()
+
+
 def test_row_movers_bound_rows():
     # a caller-supplied row id at or past max_rows is never read or written:
     # the pair is skipped, MOE_ERR_INDEX is raised, and canary rows past the
