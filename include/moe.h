@@ -277,8 +277,8 @@ MOE_API int32_t moe_grouped_ffn_variant(int32_t E, int32_t D, int32_t F,
  * device that cannot host the grid fails the call with MOE_ERR_CUDA instead
  * of stalling.  Experts with many rows run on SM pairs instead
  * (moe_grouped_ffn_variant), which claim tiles in order and need no
- * co-residency; max_ctas is then rounded down to whole pairs.  MOE_F32 runs
- * fp32 FMA (max_ctas unused). */
+ * co-residency; max_ctas is then rounded down to whole pairs, one pair (2
+ * CTAs) at least.  MOE_F32 runs fp32 FMA (max_ctas unused). */
 MOE_API moe_status moe_grouped_ffn(int32_t E, int32_t D, int32_t F, int32_t max_rows,
                            int32_t dtype, const void* xp,
                            const int32_t* expert_offsets, const void* w13,
