@@ -239,8 +239,8 @@ def launches_per_step(layer, routed):
     # layout (one block, or histogram + scan + assignment), permute, combine
     n = L.moe_dispatch_layout_launches(layer.T, layer.k, layer.E) + 1 + 1
     if routed:
-        # route: one warp-per-token kernel up to 32 experts, else the router
-        # GEMM and the select kernel
+        # route: one kernel up to 32 experts (moe_route_launches says when),
+        # else the router GEMM and the select kernel
         n += L.moe_route_launches(layer.cfg)
     if not layer.identity:
         # grouped FFN: bf16 up and down in one tcgen05 launch; fp32 as two
@@ -315,7 +315,9 @@ def kernel_label(layer, key):
                 3: "moe_grouped_ffn (one tcgen05 launch, up + down, SM pairs "
                    "on 256-row tiles)"}.get(ffn_variant(layer),
                                             "moe_grouped_ffn"),
-        "route": ("moe_route (one warp-per-token kernel)"
+        "route": (("moe_route (one kernel: 16-token tiles on the warp-level "
+                   "MMA)" if layer.cfg.dtype == L.MOE_BF16 else
+                   "moe_route (one warp-per-token kernel)")
                   if L.moe_route_launches(layer.cfg) == 1 else
                   "moe_route (router GEMM + select)"),
         "layout": f"moe_dispatch_layout ({n_layout} launch"

@@ -29,7 +29,7 @@ struct RoutePlan {
   size_t ws_bytes;   // partial logits [splits][T][E] fp32
 };
 RoutePlan plan_route(const moe_route_cfg& c, int num_sms);
-bool route_single_kernel(const moe_route_cfg& c);
+bool route_single_kernel(const moe_route_cfg& c, int num_sms);
 
 struct RouteSelectArgs {
   int T, E, k, score, n_groups, topk_groups, group_score_topk, splits;

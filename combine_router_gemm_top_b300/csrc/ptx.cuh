@@ -102,20 +102,19 @@ __device__ __forceinline__ void bulk_load_g2s(void* dst, const void* src,
       : "memory");
 }
 
-// acc + x.lo * w.lo, then + x.hi * w.hi, for bf16 pairs packed in 32 bits:
-// the mixed-precision FMA takes bf16 factors and an fp32 addend.  A product
-// of two bf16 values is exact in fp32, so each step rounds exactly as fmaf
-// on the widened factors does.
-__device__ __forceinline__ float fma_bf16x2_f32(uint32_t x, uint32_t w,
-                                                float acc) {
-  asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
-      "mov.b32 {xl, xh}, %1;\n\t"
-      "mov.b32 {wl, wh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, xl, wl, %0;\n\t"
-      "fma.rn.f32.bf16 %0, xh, wh, %0;\n\t}"
-      : "+f"(acc)
-      : "r"(x), "r"(w));
-  return acc;
+// d += A x B on one warp: A is 16 x 16 bf16 (registers a0..a3 hold, for lane
+// (g, t) = (lane / 4, lane % 4), the K pairs 2t, 2t + 1 of rows g and g + 8,
+// then the K pairs 2t + 8, 2t + 9 of the same rows), B is 16 x 8 bf16 (b0, b1:
+// K pairs 2t, 2t + 1 and 2t + 8, 2t + 9 of column g), d is 16 x 8 fp32 (rows
+// g and g + 8, columns 2t and 2t + 1).
+__device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0,
+                                                  uint32_t a1, uint32_t a2,
+                                                  uint32_t a3, uint32_t b0,
+                                                  uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // ---------------------------------------------------------------- tcgen05

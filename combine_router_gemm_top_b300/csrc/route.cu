@@ -1,12 +1,11 @@
 // moe_route kernels: router GEMM (tcgen05 split-K for bf16, fp32 FMA for
 // fp32), then per-token scoring, group-limited top-k and gates; for up to
-// 32 experts with a small W_r, both in one warp-per-token kernel
+// 32 experts, both in one kernel (bf16: 16 tokens a block on the warp-level
+// MMA; fp32 with a small W_r: one warp per token on the FMA pipes)
 // ("Expert Parallelism in LLMs", The Execution Pipeline, step 1 "Router
 // Gating and Softmax Selection": g_t = Softmax(TopK(W_g x_t, k))).
 #include <cuda.h>
 #include <float.h>
-
-#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -491,14 +490,14 @@ __global__ void __launch_bounds__(kSelWarps * 32)
   select_token<NI>(a, t, lane, lg, skey[warp]);
 }
 
-// The whole router for small E x D in one kernel, one warp per token.  One
-// thread copies W_r (E x D) into shared memory with a single bulk copy while
-// the warps' first x vectors are in flight; rows E..EP-1 are zero so that the
-// expert loop has no branch.  Lane l owns the token's 16-byte vectors l,
-// l + 32, ..., accumulates the EP dot products in fp32 on the FMA pipes, a
-// shuffle tree adds the lanes' parts, and lane e keeps expert e's logit for
-// the selection.  For few experts this replaces a tensor-core GEMM split many
-// ways plus a separate select launch.
+// The whole fp32 router for small E x D in one kernel, one warp per token.
+// One thread copies W_r (E x D) into shared memory with a single bulk copy
+// while the warps' first x vectors are in flight; rows E..EP-1 are zero so
+// that the expert loop has no branch.  Lane l owns the token's 16-byte
+// vectors l, l + 32, ..., accumulates the EP dot products in fp32 on the FMA
+// pipes, a shuffle tree adds the lanes' parts, and lane e keeps expert e's
+// logit for the selection.  For few experts this replaces a router GEMM plus
+// a separate select launch.
 template <typename T, int EP>
 __global__ void __launch_bounds__(kSelWarps * 32)
     route_warp_kernel(RouteSelectArgs a, const T* __restrict__ x,
@@ -556,25 +555,14 @@ __global__ void __launch_bounds__(kSelWarps * 32)
     for (int u = 0; u < U; ++u) {
       const int v = v0 + 32 * u;
       if (v < nvec) {
-        if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-          const uint32_t xw[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
+        float xf[N];
+        Vec16<T>::to_f32(cur[u], xf);
 #pragma unroll
-          for (int e = 0; e < EP; ++e) {
-            const uint4 wv = wsm[e * nvec + v];
-            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+        for (int e = 0; e < EP; ++e) {
+          float wf[N];
+          Vec16<T>::to_f32(wsm[e * nvec + v], wf);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) acc[e] = fma_bf16x2_f32(xw[i], ww[i], acc[e]);
-          }
-        } else {
-          float xf[N];
-          Vec16<T>::to_f32(cur[u], xf);
-#pragma unroll
-          for (int e = 0; e < EP; ++e) {
-            float wf[N];
-            Vec16<T>::to_f32(wsm[e * nvec + v], wf);
-#pragma unroll
-            for (int i = 0; i < N; ++i) acc[e] = fmaf(xf[i], wf[i], acc[e]);
-          }
+          for (int i = 0; i < N; ++i) acc[e] = fmaf(xf[i], wf[i], acc[e]);
         }
       }
     }
@@ -586,6 +574,109 @@ __global__ void __launch_bounds__(kSelWarps * 32)
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d);
     if (lane == e) lg[0] = s;
+  }
+  select_token<1>(a, t, lane, lg, skey[warp]);
+}
+
+// The bf16 router for up to 32 experts in one kernel, on the warp-level MMA.
+// A block takes 16 tokens and its 16 warps split D between them; each warp
+// accumulates a 16-token x EP-expert tile with m16n8k16 MMAs whose operands
+// come straight from global memory into registers.  A dot product may take
+// its D terms in any order, so lane (g, t) loads the 16 bytes at elements
+// 8t..8t+7 of each 32-element chunk of token rows g and g + 8 and of expert
+// row g, and hands elements 8t..8t+3 to one MMA and 8t+4..8t+7 to a second
+// as their K pairs (2t, 2t+1) and (2t+8, 2t+9).  A and B see the same
+// permutation of K, every load is 16 bytes, and the four lanes of a row read
+// 64 contiguous bytes.  W_r is read once per block (from L2) instead of once
+// per token from shared memory.  The warps' partial tiles are added in warp
+// order, so a token's logits do not depend on the batch it is in; warp w then
+// runs the selection for token w.
+constexpr int kMmaRouteTok = 16;
+constexpr int kMmaRouteWarps = 16;
+constexpr int kMmaRouteKey = 64;   // per-warp selection scratch (E <= 32)
+static_assert(kMmaRouteTok == kMmaRouteWarps, "warp w selects token w");
+
+template <int EP>
+__global__ void __launch_bounds__(kMmaRouteWarps * 32, 1)
+    route_mma_kernel(RouteSelectArgs a, const __nv_bfloat16* __restrict__ x,
+                     const __nv_bfloat16* __restrict__ w, int D, int tb) {
+  constexpr int NB = EP / 8;            // n tiles of 8 experts
+  constexpr int U = 24 / (2 + NB);      // chunks in flight: 96 registers of loads
+  __shared__ float part[kMmaRouteWarps][kMmaRouteTok][EP];
+  __shared__ float skey[kMmaRouteWarps][kMmaRouteKey];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const int q = lane & 3;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tb;
+  const int E = a.E;
+  const int nch = (D + 31) / 32;
+  const int per = (nch + kMmaRouteWarps - 1) / kMmaRouteWarps;
+  const int c_begin = warp * per;
+  const int c_end = min(nch, c_begin + per);
+  const bool lo_ok = g < tb && t0 + g < a.T;
+  const bool hi_ok = g + 8 < tb && t0 + g + 8 < a.T;
+  const __nv_bfloat16* xlo = x + (lo_ok ? t0 + g : 0) * D + 8 * q;
+  const __nv_bfloat16* xhi = x + (hi_ok ? t0 + g + 8 : 0) * D + 8 * q;
+  const __nv_bfloat16* wr[NB];
+  bool w_ok[NB];
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+    w_ok[j] = 8 * j + g < E;
+    wr[j] = w + static_cast<int64_t>(w_ok[j] ? 8 * j + g : 0) * D + 8 * q;
+  }
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  float acc[2][NB][4];   // even and odd chunks: two MMA chains
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[h][j][i] = 0.0f;
+
+  for (int c0 = c_begin; c0 < c_end; c0 += U) {
+    uint4 ra[U][2], rb[U][NB];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u;
+      const bool ok = c < c_end && 32 * c + 8 * q < D;
+      ra[u][0] = ok && lo_ok ? ld_nc_v4(xlo + 32 * c) : zero;
+      ra[u][1] = ok && hi_ok ? ld_nc_v4(xhi + 32 * c) : zero;
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+        rb[u][j] = ok && w_ok[j]
+                       ? __ldg(reinterpret_cast<const uint4*>(wr[j] + 32 * c))
+                       : zero;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (c0 + u < c_end) {   // warp-uniform
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          mma_m16n8k16_bf16(acc[u & 1][j], ra[u][0].x, ra[u][1].x,
+                            ra[u][0].y, ra[u][1].y, rb[u][j].x, rb[u][j].y);
+          mma_m16n8k16_bf16(acc[u & 1][j], ra[u][0].z, ra[u][1].z,
+                            ra[u][0].w, ra[u][1].w, rb[u][j].z, rb[u][j].w);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+    const int e = 8 * j + 2 * q;
+    part[warp][g][e] = __fadd_rn(acc[0][j][0], acc[1][j][0]);
+    part[warp][g][e + 1] = __fadd_rn(acc[0][j][1], acc[1][j][1]);
+    part[warp][g + 8][e] = __fadd_rn(acc[0][j][2], acc[1][j][2]);
+    part[warp][g + 8][e + 1] = __fadd_rn(acc[0][j][3], acc[1][j][3]);
+  }
+  __syncthreads();
+  const int64_t t = t0 + warp;
+  if (warp >= tb || t >= a.T) return;
+  float lg[1] = {0.0f};
+  if (lane < EP) {
+#pragma unroll
+    for (int v = 0; v < kMmaRouteWarps; ++v)
+      lg[0] = __fadd_rn(lg[0], part[v][warp][lane]);
   }
   select_token<1>(a, t, lane, lg, skey[warp]);
 }
@@ -646,14 +737,24 @@ RoutePlan plan_route(const moe_route_cfg& c, int num_sms) {
   return p;
 }
 
-// Up to 32 experts, with W_r small enough to sit in shared memory, the router
-// is one warp-per-token kernel on the FMA pipes; otherwise the tensor-core
-// GEMM then the select kernel.
+// Up to 32 experts the router can be one kernel.  In bf16 that is the MMA
+// kernel, which reads its operands straight from global memory: every block
+// reads all of W_r (EP/16 times its tile's x bytes, from L2), so it is taken
+// for up to 8 experts, for W_r of at most 96 KiB, or while the tokens fill at
+// most one 16-token tile per SM; beyond that the split-K GEMM, which reads
+// W_r once per 128-token tile, is faster (T = 16384, 32 experts, D = 4096:
+// 47 against 57 us).  In fp32 it is the warp-per-token kernel on the FMA
+// pipes when W_r fits in shared memory.  Otherwise the router GEMM (tensor
+// cores in bf16), then the select kernel.
 constexpr int kWarpRouteSmem = 96 * 1024;
 static int route_ep(int E) { return E <= 8 ? 8 : E <= 16 ? 16 : 32; }
-bool route_single_kernel(const moe_route_cfg& c) {
-  return c.E <= 32 && static_cast<int64_t>(route_ep(c.E)) * c.D *
-                              dtype_bytes(c.dtype) <= kWarpRouteSmem;
+bool route_single_kernel(const moe_route_cfg& c, int num_sms) {
+  if (c.E > 32) return false;
+  const bool small_w = static_cast<int64_t>(route_ep(c.E)) * c.D *
+                           dtype_bytes(c.dtype) <= kWarpRouteSmem;
+  if (c.dtype != MOE_BF16) return small_w;
+  return c.E <= 8 || small_w ||
+         static_cast<int64_t>(c.T) <= static_cast<int64_t>(kMmaRouteTok) * num_sms;
 }
 
 template <typename T, int EP>
@@ -670,14 +771,39 @@ static bool launch_route_warp_ep(const RouteSelectArgs& s, const T* x,
   return true;
 }
 
-template <typename T>
-static bool launch_route_warp(const RouteSelectArgs& s, const void* x,
-                              const void* w_r, int D, cudaStream_t stream) {
-  const T* xx = static_cast<const T*>(x);
-  const T* ww = static_cast<const T*>(w_r);
-  if (s.E <= 8) return launch_route_warp_ep<T, 8>(s, xx, ww, D, stream);
-  if (s.E <= 16) return launch_route_warp_ep<T, 16>(s, xx, ww, D, stream);
-  return launch_route_warp_ep<T, 32>(s, xx, ww, D, stream);
+// Tokens per block: 16, or fewer when that leaves SMs without a block (the
+// MMA tile's remaining rows load nothing).
+static int route_mma_tokens(int T, int num_sms) {
+  const int64_t per = ceil_div(T, num_sms > 0 ? num_sms : 1);
+  return per >= kMmaRouteTok ? kMmaRouteTok : per < 1 ? 1 : static_cast<int>(per);
+}
+
+template <int EP>
+static void launch_route_mma_ep(const RouteSelectArgs& s,
+                                const __nv_bfloat16* x,
+                                const __nv_bfloat16* w, int D, int num_sms,
+                                cudaStream_t stream) {
+  const int tb = route_mma_tokens(s.T, num_sms);
+  const unsigned grid = static_cast<unsigned>(ceil_div(s.T, tb));
+  route_mma_kernel<EP><<<grid, kMmaRouteWarps * 32, 0, stream>>>(s, x, w, D, tb);
+}
+
+static bool launch_route_warp(const RouteSelectArgs& s, int32_t dtype,
+                              const void* x, const void* w_r, int D,
+                              int num_sms, cudaStream_t stream) {
+  if (dtype == MOE_BF16) {
+    const auto* xx = static_cast<const __nv_bfloat16*>(x);
+    const auto* ww = static_cast<const __nv_bfloat16*>(w_r);
+    if (s.E <= 8) launch_route_mma_ep<8>(s, xx, ww, D, num_sms, stream);
+    else if (s.E <= 16) launch_route_mma_ep<16>(s, xx, ww, D, num_sms, stream);
+    else launch_route_mma_ep<32>(s, xx, ww, D, num_sms, stream);
+    return true;
+  }
+  const auto* xx = static_cast<const float*>(x);
+  const auto* ww = static_cast<const float*>(w_r);
+  if (s.E <= 8) return launch_route_warp_ep<float, 8>(s, xx, ww, D, stream);
+  if (s.E <= 16) return launch_route_warp_ep<float, 16>(s, xx, ww, D, stream);
+  return launch_route_warp_ep<float, 32>(s, xx, ww, D, stream);
 }
 
 moe_status launch_route(const moe_route_cfg& c, const void* x, const void* w_r,
@@ -685,7 +811,7 @@ moe_status launch_route(const moe_route_cfg& c, const void* x, const void* w_r,
                         int32_t* topk_idx, float* topk_gate, float* logits_out,
                         void* ws, int32_t* status, cudaStream_t stream,
                         int num_sms) {
-  if (route_single_kernel(c)) {
+  if (route_single_kernel(c, num_sms)) {
     RouteSelectArgs s{};
     s.T = c.T;
     s.E = c.E;
@@ -701,10 +827,8 @@ moe_status launch_route(const moe_route_cfg& c, const void* x, const void* w_r,
     s.topk_gate = topk_gate;
     s.logits_out = logits_out;
     s.status = status;
-    const bool ok = c.dtype == MOE_BF16
-                        ? launch_route_warp<__nv_bfloat16>(s, x, w_r, c.D, stream)
-                        : launch_route_warp<float>(s, x, w_r, c.D, stream);
-    if (!ok) return MOE_ERR_CUDA;
+    if (!launch_route_warp(s, c.dtype, x, w_r, c.D, num_sms, stream))
+      return MOE_ERR_CUDA;
     return launch_status();
   }
   const RoutePlan p = plan_route(c, num_sms);

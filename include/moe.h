@@ -115,11 +115,16 @@ typedef struct {
  * split-K router GEMM).  Returns 0 for an invalid cfg. */
 MOE_API size_t moe_route_workspace_size(const moe_route_cfg* cfg);
 
-/* Kernels one moe_route call launches for `cfg`: 1 when E <= 32 and W_r,
- * padded to 8, 16 or 32 rows, takes at most 96 KiB (one warp per token
- * computes the logits on the CUDA cores from W_r in shared memory and
- * selects), else 2 (the router GEMM, then the select kernel); 0 for an
- * invalid cfg or T = 0.  Host only. */
+/* Kernels one moe_route call launches for `cfg`: 1 when E <= 32 and
+ *   bf16: E <= 8, or W_r padded to 8, 16 or 32 rows takes at most 96 KiB,
+ *         or T <= 16 x the current device's SM count (blocks of up to 16
+ *         tokens compute the logits on the warp-level MMA, operands read
+ *         straight from global memory, then select);
+ *   fp32: W_r padded to 8, 16 or 32 rows takes at most 96 KiB (one warp per
+ *         token computes the logits on the CUDA cores from W_r in shared
+ *         memory and selects);
+ * else 2 (the router GEMM, then the select kernel); 0 for an invalid cfg or
+ * T = 0.  Host only. */
 MOE_API int32_t moe_route_launches(const moe_route_cfg* cfg);
 
 /* moe_route -- router GEMM, score, top-k and gates

@@ -243,14 +243,17 @@ ROUTE_CASES = [
     (300, 64, 40, 3, torch.float32, "softmax_topk", (1, 1, 0), 0.02, None, None),
     # 32 experts exactly: the one-kernel router at its widest
     (700, 1024, 32, 4, torch.bfloat16, "softmax_full", (1, 1, 0), None, 1.5, None),
-    # one-kernel router: W_r exactly at its 96 KiB shared-memory limit; 5
-    # experts padded to 8 zero rows with a ragged vector count (D = 520);
-    # 12 experts (16 rows) with the group limit
+    # one-kernel router: bf16 over 24 chunks per warp (two load batches);
+    # fp32 W_r exactly at its 96 KiB shared-memory limit; 5 experts padded
+    # to 8 zero rows with a ragged chunk count (D = 520); 12 experts (16
+    # rows) with the group limit
     (150, 6144, 8, 2, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
+    (150, 3072, 8, 2, torch.float32, "softmax_topk", (1, 1, 0), 0.02, None, None),
     (333, 520, 5, 2, torch.bfloat16, "softmax_full", (1, 1, 0), None, 1.0, None),
     (200, 320, 12, 3, torch.bfloat16, "sigmoid_bias", (4, 2, 2), None, None, 0.1),
-    # few experts but W_r over that limit: the router GEMM (bf16 on tensor
-    # cores, fp32 on the FMA pipes), then the select kernel
+    # few experts, long rows: bf16 stays on the one-kernel router (32
+    # chunks per warp, several load batches); fp32 W_r over the 96 KiB
+    # shared-memory limit takes the FMA router GEMM, then the select kernel
     (257, 8192, 8, 2, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
     (130, 4096, 8, 2, torch.float32, "softmax_topk", (1, 1, 0), 0.02, None, None),
     # group scores over more than 8 keys (the warp-round path)
@@ -269,8 +272,9 @@ ROUTE_CASES = [
     # more row blocks than SMs, unevenly: the GEMM runs as two K halves
     (20000, 512, 64, 4, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
     (10000, 128, 64, 4, torch.bfloat16, "softmax_topk", (4, 2, 2), None, None, None),
-    # one-kernel router over more than one block per SM (T above 8 warps per
-    # SM), odd T: 8, 16 and 32 expert rows, bf16 and fp32, every score mode
+    # one-kernel router at and above one block per SM, odd T (bf16: token
+    # tiles of 14 and 16 rows with a ragged last tile; fp32: more than 8 warps
+    # per SM): 8, 16 and 32 expert rows, every score mode
     (2049, 4096, 8, 2, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
     (1999, 256, 32, 4, torch.bfloat16, "softmax_full", (1, 1, 0), None, 1.5, None),
     (3001, 520, 12, 3, torch.bfloat16, "sigmoid_bias", (4, 2, 2), None, None, 0.1),
