@@ -32,26 +32,57 @@ __device__ __forceinline__ int find_expert(const int32_t* off, int E, int row) {
   return lo;
 }
 
+// One warp per row and kFpw consecutive outputs: the lanes stride over the
+// dot products' length, so every load of x, H and the weight rows is
+// coalesced and each x (H) element loaded serves kFpw outputs; a shuffle tree
+// adds the lanes' parts in a fixed order.
+constexpr int kFpw = 4;
+
+__device__ __forceinline__ float warp_sum_f32(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 __global__ void ffn_up_f32_kernel(int E, int D, int F, int max_rows,
                                   const float* __restrict__ xp,
                                   const int32_t* __restrict__ off,
                                   const float* __restrict__ w13,
                                   float* __restrict__ h) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t i =
+      (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
   const int n_rows = min(__ldg(off + E), max_rows);
-  if (i >= static_cast<int64_t>(n_rows) * F) return;
-  const int row = static_cast<int>(i / F);
-  const int f = static_cast<int>(i - static_cast<int64_t>(row) * F);
+  const int fg = (F + kFpw - 1) / kFpw;   // feature groups per row
+  if (i >= static_cast<int64_t>(n_rows) * fg) return;   // warp-uniform
+  const int row = static_cast<int>(i / fg);
+  const int f0 = static_cast<int>(i - static_cast<int64_t>(row) * fg) * kFpw;
   const int e = find_expert(off, E, row);
   const float* x = xp + static_cast<int64_t>(row) * D;
-  const float* w1 = w13 + (static_cast<int64_t>(e) * 2 * F + f) * D;
+  const float* w1 = w13 + (static_cast<int64_t>(e) * 2 * F + f0) * D;
   const float* w3 = w1 + static_cast<int64_t>(F) * D;
-  float g = 0.0f, u = 0.0f;
-  for (int d = 0; d < D; ++d) {
-    g = fmaf(x[d], w1[d], g);
-    u = fmaf(x[d], w3[d], u);
+  const int nf = min(kFpw, F - f0);
+  float g[kFpw], u[kFpw];
+#pragma unroll
+  for (int j = 0; j < kFpw; ++j) g[j] = u[j] = 0.0f;
+  for (int d = lane; d < D; d += 32) {
+    const float xv = __ldg(x + d);
+#pragma unroll
+    for (int j = 0; j < kFpw; ++j) {
+      if (j < nf) {
+        g[j] = fmaf(xv, __ldg(w1 + static_cast<int64_t>(j) * D + d), g[j]);
+        u[j] = fmaf(xv, __ldg(w3 + static_cast<int64_t>(j) * D + d), u[j]);
+      }
+    }
   }
-  h[i] = g / (1.0f + expf(-g)) * u;
+  float out = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kFpw; ++j) {
+    const float gs = warp_sum_f32(g[j]);
+    const float us = warp_sum_f32(u[j]);
+    if (lane == j) out = gs / (1.0f + expf(-gs)) * us;
+  }
+  if (lane < nf) h[static_cast<int64_t>(row) * F + f0 + lane] = out;
 }
 
 __global__ void ffn_down_f32_kernel(int E, int D, int F, int max_rows,
@@ -59,17 +90,35 @@ __global__ void ffn_down_f32_kernel(int E, int D, int F, int max_rows,
                                     const int32_t* __restrict__ off,
                                     const float* __restrict__ w2,
                                     float* __restrict__ yp) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t i =
+      (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
   const int n_rows = min(__ldg(off + E), max_rows);
-  if (i >= static_cast<int64_t>(n_rows) * D) return;
-  const int row = static_cast<int>(i / D);
-  const int d = static_cast<int>(i - static_cast<int64_t>(row) * D);
+  const int dg = (D + kFpw - 1) / kFpw;   // output groups per row
+  if (i >= static_cast<int64_t>(n_rows) * dg) return;   // warp-uniform
+  const int row = static_cast<int>(i / dg);
+  const int d0 = static_cast<int>(i - static_cast<int64_t>(row) * dg) * kFpw;
   const int e = find_expert(off, E, row);
   const float* hr = h + static_cast<int64_t>(row) * F;
-  const float* w = w2 + (static_cast<int64_t>(e) * D + d) * F;
-  float acc = 0.0f;
-  for (int f = 0; f < F; ++f) acc = fmaf(hr[f], w[f], acc);
-  yp[i] = acc;
+  const float* w = w2 + (static_cast<int64_t>(e) * D + d0) * F;
+  const int nd = min(kFpw, D - d0);
+  float acc[kFpw];
+#pragma unroll
+  for (int j = 0; j < kFpw; ++j) acc[j] = 0.0f;
+  for (int f = lane; f < F; f += 32) {
+    const float hv = __ldg(hr + f);
+#pragma unroll
+    for (int j = 0; j < kFpw; ++j)
+      if (j < nd)
+        acc[j] = fmaf(hv, __ldg(w + static_cast<int64_t>(j) * F + f), acc[j]);
+  }
+  float out = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kFpw; ++j) {
+    const float s = warp_sum_f32(acc[j]);
+    if (lane == j) out = s;
+  }
+  if (lane < nd) yp[static_cast<int64_t>(row) * D + d0 + lane] = out;
 }
 
 // ----------------------------------------------------------- host
@@ -183,13 +232,16 @@ moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
   if (max_rows == 0) return MOE_OK;
   if (dtype == MOE_F32) {
     float* h = static_cast<float*>(ws);
-    const int64_t n1 = static_cast<int64_t>(max_rows) * F;
-    ffn_up_f32_kernel<<<static_cast<unsigned>(ceil_div(n1, 256)), 256, 0,
+    // one warp per row and kFpw outputs, 8 warps a block
+    const int64_t n1 = static_cast<int64_t>(max_rows) * ceil_div(F, kFpw);
+    const int64_t n2 = static_cast<int64_t>(max_rows) * ceil_div(D, kFpw);
+    if (ceil_div(n1, 8) > INT32_MAX || ceil_div(n2, 8) > INT32_MAX)
+      return MOE_ERR_UNSUPPORTED;
+    ffn_up_f32_kernel<<<static_cast<unsigned>(ceil_div(n1, 8)), 256, 0,
                         stream>>>(E, D, F, max_rows,
                                   static_cast<const float*>(xp), offsets,
                                   static_cast<const float*>(w13), h);
-    const int64_t n2 = static_cast<int64_t>(max_rows) * D;
-    ffn_down_f32_kernel<<<static_cast<unsigned>(ceil_div(n2, 256)), 256, 0,
+    ffn_down_f32_kernel<<<static_cast<unsigned>(ceil_div(n2, 8)), 256, 0,
                           stream>>>(E, D, F, max_rows, h, offsets,
                                     static_cast<const float*>(w2),
                                     static_cast<float*>(yp));

@@ -280,6 +280,10 @@ ROUTE_CASES = [
     (3001, 520, 12, 3, torch.bfloat16, "sigmoid_bias", (4, 2, 2), None, None, 0.1),
     (1501, 96, 24, 5, torch.float32, "sigmoid_bias", (3, 2, 2), None, None, 0.05),
     (1301, 64, 16, 4, torch.float32, "softmax_topk", (1, 1, 0), 0.02, None, None),
+    # bf16, 16 and 32 experts with W_r over 96 KiB: the MMA router while T
+    # fits one 16-token tile per SM, the router GEMM (16 columns) above that
+    (2300, 4096, 32, 4, torch.bfloat16, "softmax_full", (1, 1, 0), None, 1.5, None),
+    (3000, 4096, 16, 4, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
 ]
 
 
@@ -462,6 +466,8 @@ FFN_CASES = [
     (5, 192, 256, [7, 0, 0, 130, 64], torch.bfloat16),
     (8, 1024, 512, [100, 300, 0, 17, 128, 129, 255, 1], torch.bfloat16),
     (8, 64, 128, [10, 50, 0, 3, 128, 70, 1, 250], torch.float32),
+    # fp32 with D and F not multiples of a warp's 32 lanes
+    (3, 36, 100, [5, 40, 33], torch.float32),
     # tails of every swapped MMA width (16..112) and the 112/113 switch to
     # the normal tile; D = 320 leaves a down-projection tile half outside D
     (8, 256, 256, [16, 33, 112, 113, 128 + 48, 256 + 97, 240, 2],
