@@ -249,20 +249,22 @@ def launches_per_step(layer, routed):
     return n
 
 
-def kernel_models(wl, n_kept, es, peaks, active_experts=None):
+def kernel_models(wl, n_kept, es, peaks, active_experts=None, t_kept=None):
     """Algorithmic work of each step and the roofline time it implies.
     Bytes count each input read once and each output written once;
     intermediates (split-K partial logits, the SwiGLU activations H) are not
-    algorithmic."""
+    algorithmic.  t_kept: tokens with at least one kept pair, the rows
+    permute reads (T when nothing is dropped)."""
     T, D, E, k, F = wl.T, wl.D, wl.E, wl.k, wl.F
     P, N = T * k, n_kept
+    Tk = T if t_kept is None else t_kept
     hbm = peaks["hbm_gbs"] * 1e9
     tc = peaks["bf16_tflops_sustained"] * 1e12
     m = {}
     m["route"] = dict(bytes=T * D * es + E * D * es + P * 8,
                       flops=2.0 * T * D * E)
     m["layout"] = dict(bytes=P * 4 + P * 4 + N * 4, flops=0.0)
-    m["permute"] = dict(bytes=T * D * es + N * D * es + P * 4, flops=0.0)
+    m["permute"] = dict(bytes=Tk * D * es + N * D * es + P * 4, flops=0.0)
     if not wl.identity_experts:
         ea = E if active_experts is None else active_experts
         m["ffn"] = dict(bytes=ea * 3 * F * D * es + 2 * N * D * es,
@@ -274,6 +276,13 @@ def kernel_models(wl, n_kept, es, peaks, active_experts=None):
         v["bound"] = "tensor" if t_tc > t_hbm else "hbm"
         v["roofline_ms"] = max(t_hbm, t_tc) * 1e3
     return m
+
+
+def tokens_kept(layer):
+    """Tokens with at least one kept pair: the x rows moe_permute reads
+    (counted after the timed region, from the layout's dst_row)."""
+    dst = layer.dst_row[:layer.T * layer.k].view(layer.T, layer.k)
+    return int((dst >= 0).any(dim=1).sum().item())
 
 
 def replica_seed(base_seed, rank):
@@ -374,7 +383,7 @@ def measure(args, wl, dev, rank, world, local_rank, dist):
     es = x.element_size()
     peaks = load_peaks()
     tc_peak, tc_note = choose_bf16_peak(peaks, wall, clk)
-    models = kernel_models(wl, n_kept, es, peaks, active)
+    models = kernel_models(wl, n_kept, es, peaks, active, tokens_kept(layer))
     kernels = {}
     for key, mdl in models.items():
         ms = parts[key] / K
@@ -683,7 +692,7 @@ def run_extras(args, local_rank, workload):
             nbytes=(rows - n_kept) * D * es)
         put("padded_permute", timed(lambda: L.moe_permute(
             T, k, D, layer.dcode, x, dst_p, xpad, layer.status)),
-            nbytes=T * D * es + n_kept * D * es + P * 4)
+            nbytes=tokens_kept(layer) * D * es + n_kept * D * es + P * 4)
         put("padded_ffn", timed(lambda: L.moe_grouped_ffn(
             E, D, wl.F, rows, layer.dcode, xpad, off_p, layer.w13, layer.w2,
             ypad, fws, st)), flops=6.0 * D * wl.F * rows)

@@ -3,9 +3,10 @@
 //
 // permute  ("Expert Parallelism in LLMs", The Execution Pipeline, step 2:
 //           tokens physically reordered into contiguous per-destination
-//           buffers) -- token-major scatter: each token row is read from
-//           HBM once and written to each kept destination row, so the
-//           traffic is T*D*s read + N*D*s written.
+//           buffers) -- token-major scatter: each token row with a kept
+//           slot is read from HBM once and written to each kept destination
+//           row, so the traffic is T_kept*D*s read + N*D*s written (T_kept:
+//           tokens with at least one kept slot).
 // combine  (same page, step 6 "Unpermutation and Weighted Reduction") --
 //           token-major gather: y[t] = sum_j g[t,j] * yp[dst_row[t*k+j]],
 //           fp32 accumulation in slot order (deterministic, no atomics),
@@ -43,6 +44,8 @@ __global__ void __launch_bounds__(kRowWarps * 32)
     // lane j < k holds the destination row of slot j
     const int32_t my_dst = checked_row(
         lane < k ? __ldg(dst_row + t * k + lane) : -1, max_rows, status);
+    // a token with no kept slot (all dropped at capacity) is not read
+    if (!__any_sync(0xffffffffu, my_dst >= 0)) continue;
     const uint4* src = x + t * nvec;
     for (int v0 = v_begin + lane; v0 < v_end; v0 += 32 * kUnroll) {
       uint4 buf[kUnroll];

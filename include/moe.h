@@ -224,8 +224,9 @@ MOE_API moe_status moe_dispatch_layout_noalloc(
 /* moe_permute -- xp[dst_row[t*k + j]] = x[t] for every kept pair
  * ("Expert Parallelism in LLMs", The Execution Pipeline, step 2: tokens
  * physically reordered into contiguous per-destination buffers).  Each
- * token row is read once and written to each of its kept destinations
- * (a scatter by dst_row, so x is read once rather than once per pair).
+ * token row with a kept pair is read once and written to each of its kept
+ * destinations (a scatter by dst_row, so x is read once rather than once per
+ * pair); the row of a token whose pairs were all dropped is not read.
  *   x         [T, D] dtype in, 16-byte aligned
  *   dst_row   [T*k] int32 in (moe_dispatch_layout's): < 0 = dropped
  *   xp        [max_rows, D] dtype out, 16-byte aligned; rows not named by

@@ -57,6 +57,19 @@ def test_switch_ffn_counts_only_active_experts(bench):
     assert part["ffn"]["flops"] == full["ffn"]["flops"]
 
 
+def test_permute_reads_only_tokens_with_a_kept_pair(bench):
+    # at capacity a token whose pairs all dropped has no row to move: permute
+    # reads t_kept rows, combine still writes all T rows of y (zeros there)
+    wl = W.WORKLOADS["switch_bf16"]
+    n, t_kept = 1753, 1753                              # k = 1
+    m = bench.kernel_models(wl, n, 2, PEAKS, t_kept=t_kept)
+    ids = wl.T * wl.k * 4
+    assert m["permute"]["bytes"] == (t_kept + n) * wl.D * 2 + ids
+    assert m["combine"]["bytes"] == (n + wl.T) * wl.D * 2 + 2 * ids
+    dropless = bench.kernel_models(wl, n, 2, PEAKS)
+    assert dropless["permute"]["bytes"] == (wl.T + n) * wl.D * 2 + ids
+
+
 def test_sweep_permute_and_combine_bytes(bench):
     wl = W.WORKLOADS["sweep_bf16_uniform_T65536"]
     n = wl.T * wl.k

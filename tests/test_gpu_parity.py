@@ -406,7 +406,9 @@ def test_sigmoid_key_bit_exact():
     (300, 8, 16, 520, torch.bfloat16, 30), (129, 2, 8, 64, torch.float32, 20),
     (2048, 8, 128, 4096, torch.bfloat16, 0),
     # rows cut into 2 segments of 192 vectors, and into 4 with drops
-    (777, 2, 8, 3072, torch.bfloat16, 0), (500, 2, 8, 2048, torch.float32, 40)])
+    (777, 2, 8, 3072, torch.bfloat16, 0), (500, 2, 8, 2048, torch.float32, 40),
+    # top-1 at capacity, most tokens dropped whole: their rows are not read
+    (4000, 1, 64, 1024, torch.bfloat16, 30)])
 def test_permute_combine_parity(T, k, E, D, dt, cap):
     idx = _idx("distinct", T, k, E, seed=D)
     lay = O.dispatch_layout(idx, E, 1, cap if cap > 0 else None)
