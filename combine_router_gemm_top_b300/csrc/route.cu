@@ -80,12 +80,13 @@ constexpr int kSelGroupTop = 8;   // per-lane scan handles group_score_topk <= 8
 // Lane g < n_groups: the fp32 sum of the m largest keys of group g (added
 // largest first) and the m-th largest key; keys of experts e = lane + 32 i
 // in key[] (-inf for none).  Lane g scans its group's keys from the warp's
-// shared scratch keeping the m largest in a sorted list (m <= 8; equal keys
-// are interchangeable for the sum).
-template <int NI>
-__device__ __forceinline__ void group_top(const float (&key)[NI], int lane,
-                                          int E, int n_groups, int gs, int m,
-                                          float* sk, float& sum, float& mth) {
+// shared scratch keeping the MT largest in a sorted list (m <= MT <= 8;
+// equal keys are interchangeable for the sum).
+template <int NI, int MT>
+__device__ __forceinline__ void group_top_mt(const float (&key)[NI], int lane,
+                                             int E, int n_groups, int gs,
+                                             int m, float* sk, float& sum,
+                                             float& mth) {
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int e = lane + 32 * i;
@@ -95,25 +96,35 @@ __device__ __forceinline__ void group_top(const float (&key)[NI], int lane,
   sum = 0.0f;
   mth = -INFINITY;
   if (lane < n_groups) {
-    float v[kSelGroupTop];
+    float v[MT];
 #pragma unroll
-    for (int j = 0; j < kSelGroupTop; ++j) v[j] = -INFINITY;
+    for (int j = 0; j < MT; ++j) v[j] = -INFINITY;
     for (int e = lane * gs; e < (lane + 1) * gs; ++e) {
       float x = sk[e + (e >> 5)];
 #pragma unroll
-      for (int j = 0; j < kSelGroupTop; ++j) {
+      for (int j = 0; j < MT; ++j) {
         const float hi = fmaxf(v[j], x);
         x = fminf(v[j], x);
         v[j] = hi;
       }
     }
 #pragma unroll
-    for (int j = 0; j < kSelGroupTop; ++j) {
+    for (int j = 0; j < MT; ++j) {
       if (j < m) sum = __fadd_rn(sum, v[j]);
       if (j == m - 1) mth = v[j];
     }
   }
   __syncwarp();
+}
+// the sorted list as short as m allows (the common m = 2 keeps two)
+template <int NI>
+__device__ __forceinline__ void group_top(const float (&key)[NI], int lane,
+                                          int E, int n_groups, int gs, int m,
+                                          float* sk, float& sum, float& mth) {
+  if (m <= 2)
+    group_top_mt<NI, 2>(key, lane, E, n_groups, gs, m, sk, sum, mth);
+  else
+    group_top_mt<NI, kSelGroupTop>(key, lane, E, n_groups, gs, m, sk, sum, mth);
 }
 
 // Lane g < n_groups: the fp32 sum of the m largest keys of group g by m
@@ -228,8 +239,8 @@ __device__ __forceinline__ void select_by_logit(const RouteSelectArgs& a,
 // fp32 approximation of the sigmoid score: expf (within 2 ulp), one add and
 // one division, so it lies within 3.5 * 2^-24 of fp32(sigmoid(l)), and an
 // approximate key fp32(approx + b) within 2^-21.5 (1 + |b|) of the exact
-// key.  The selection uses it only to rule experts out, with a margin four
-// times that bound.
+// key.  The selection trusts it only where keys lie more than twice that
+// bound, taken four times over, apart; the gates use it as it is.
 __device__ __forceinline__ float sigmoid_approx(float l) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l)));
 }
@@ -292,12 +303,30 @@ __device__ __forceinline__ void exact_sigmoid_keys(const RouteSelectArgs& a,
 }
 
 // Sigmoid mode: key = fp32(fp32(sigmoid(l)) + b_e), the sigmoid in float64.
-// Every expert gets the cheap approximate key; exact keys are evaluated only
-// for the experts that can still matter.  An expert whose approximate key
-// is more than twice the error bound below the m-th largest approximate key
-// of its group (or the k-th largest among the eligible experts) lies below
-// at least m (or k) experts whatever the exact keys are, so it can neither
-// add to its group's score nor be selected, ties included.
+// Float64 runs at a small fraction of the fp32 rate on this part, so every
+// expert gets the cheap approximate key, within delta = 2^-19 (1 + max|b|)
+// of its exact key, and exact keys are evaluated only where the approximate
+// ones cannot decide.  Two approximate keys more than 2 delta ("slack")
+// apart are ordered as their exact keys are, and an expert whose approximate
+// key is more than slack from every other candidate's compares correctly
+// with exact keys too, so only candidates within slack of another one need
+// their exact key.
+//   Groups: a group score (sum of the m largest keys) from approximate keys
+//   lies within eps_g of the exact one; when the weakest chosen group leads
+//   the strongest other group by more than 2 eps_g the chosen set is
+//   certain, otherwise the exact scores are formed from exact keys of each
+//   group's candidates (those within slack of its m-th approximate key).
+//   Top-k: the eligible experts are taken in approximate-key order down to
+//   slack below the k-th (the candidates; an expert further below lies under
+//   k others whatever the exact keys are), and the candidates within slack
+//   of a neighbour in that order get exact keys before the final rounds.
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1)
+    v = fminf(v, __shfl_xor_sync(0xffffffffu, v, d));
+  return v;
+}
+
 template <int NI>
 __device__ __forceinline__ void select_by_sigmoid(const RouteSelectArgs& a,
                                                   int lane,
@@ -320,32 +349,47 @@ __device__ __forceinline__ void select_by_sigmoid(const RouteSelectArgs& a,
     bmax = fmaxf(bmax, fabsf(b));
   }
   bmax = warp_max(bmax);
-  const float slack = 2.0f * kSigmoidKeySlack * (1.0f + bmax);
+  const float delta = kSigmoidKeySlack * (1.0f + bmax);
+  const float slack = 2.0f * delta;
 
   if (a.n_groups > 1) {
     const int gs = E / a.n_groups;
     const float inv_gs = 1.0f / static_cast<float>(gs);
     const int m = a.group_score_topk;
     float gscore, mth;
+    uint32_t chosen;
     if (m <= kSelGroupTop) {
-      // exact keys for each group's candidates, then the exact group scores
-      // from those alone
       group_top<NI>(ka, lane, E, a.n_groups, gs, m, sk, gscore, mth);
-      const float thr_own = mth - slack;
+      chosen = choose_groups(gscore, lane, a.n_groups, a.topk_groups);
+      // m keys off by delta each, and the m - 1 fp32 additions of either
+      // sum rounding by at most 2^-24 of a partial sum below m (1 + max|b|)
+      const float eps_g = static_cast<float>(m) * delta +
+                          2.0f * static_cast<float>((m - 1) * m) *
+                              5.9604645e-8f * (1.0f + bmax);
+      const bool grp = lane < a.n_groups;
+      const bool in = grp && ((chosen >> lane) & 1u);
+      const float lo_in = warp_min(in ? gscore : INFINITY);
+      const float hi_out = warp_max(grp && !in ? gscore : -INFINITY);
+      if (!(lo_in - hi_out > 2.0f * eps_g)) {
+        // exact keys for each group's candidates, then the exact group
+        // scores from those alone
+        const float thr_own = mth - slack;
 #pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        const int g = group_of(lane + 32 * i, inv_gs);
-        const float thr = __shfl_sync(0xffffffffu, thr_own, g & 31);
-        need[i] = elig[i] && ka[i] >= thr;
-      }
-      exact_sigmoid_keys<NI>(a, lane, lg, need, key);
-      float kc[NI];
+        for (int i = 0; i < NI; ++i) {
+          const int g = group_of(lane + 32 * i, inv_gs);
+          const float thr = __shfl_sync(0xffffffffu, thr_own, g & 31);
+          need[i] = elig[i] && ka[i] >= thr;
+        }
+        exact_sigmoid_keys<NI>(a, lane, lg, need, key);
+        float kc[NI];
 #pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        exact[i] = need[i];
-        kc[i] = exact[i] ? key[i] : -INFINITY;
+        for (int i = 0; i < NI; ++i) {
+          exact[i] = need[i];
+          kc[i] = exact[i] ? key[i] : -INFINITY;
+        }
+        group_top<NI>(kc, lane, E, a.n_groups, gs, m, sk, gscore, mth);
+        chosen = choose_groups(gscore, lane, a.n_groups, a.topk_groups);
       }
-      group_top<NI>(kc, lane, E, a.n_groups, gs, m, sk, gscore, mth);
     } else {
       // wider group scores: exact keys for every expert
 #pragma unroll
@@ -358,44 +402,78 @@ __device__ __forceinline__ void select_by_sigmoid(const RouteSelectArgs& a,
         code[i] = elig[i] ? key_code(key[i]) : 0u;
       }
       gscore = group_sum_rounds<NI>(key, code, lane, a.n_groups, inv_gs, m);
+      chosen = choose_groups(gscore, lane, a.n_groups, a.topk_groups);
     }
-    const uint32_t chosen = choose_groups(gscore, lane, a.n_groups,
-                                          a.topk_groups);
 #pragma unroll
     for (int i = 0; i < NI; ++i)
       if (elig[i] && !((chosen >> group_of(lane + 32 * i, inv_gs)) & 1u))
         elig[i] = false;
   }
 
-  // the k-th largest approximate key among the eligible experts
+  // the eligible experts in approximate-key order down to slack below the
+  // k-th: lane r holds the r-th (up to 32)
   uint32_t ca[NI];
 #pragma unroll
   for (int i = 0; i < NI; ++i) ca[i] = elig[i] ? key_code(ka[i]) : 0u;
   float tk = -INFINITY;
-  for (int j = 0; j < a.k; ++j) {
+  int n_ord = 0;
+  bool many = false;   // more than 32 candidates
+  int ord_e = -1;
+  float ord_k = -INFINITY, ord_l = 0.0f;
+  for (int r = 0;; ++r) {
     const int w = warp_argmax<NI>(ca, lane);
-    if (w < 0) {
-      tk = -INFINITY;   // fewer than k eligible: all of them stay
-      break;
-    }
-    float mine = 0.0f;
+    if (w < 0) break;   // every eligible expert taken
+    float mine = 0.0f, mine_l = 0.0f;
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
       if (lane + 32 * i == w) {
         mine = ka[i];
+        mine_l = lg[i];
         ca[i] = 0u;
       }
     }
-    tk = __shfl_sync(0xffffffffu, mine, w & 31);
+    const float kw = __shfl_sync(0xffffffffu, mine, w & 31);
+    const float lw = __shfl_sync(0xffffffffu, mine_l, w & 31);
+    if (r >= a.k && kw < tk - slack) break;
+    if (r == a.k - 1) tk = kw;
+    if (r == 32) {
+      many = true;
+      break;
+    }
+    if (lane == r) {
+      ord_e = w;
+      ord_k = kw;
+      ord_l = lw;
+    }
+    n_ord = r + 1;
   }
   const float thr = tk - slack;
-  uint32_t code[NI];
+  if (many) {
+    // exact keys for every candidate
 #pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    const bool cand = elig[i] && ka[i] >= thr;
-    need[i] = cand && !exact[i];
+    for (int i = 0; i < NI; ++i) need[i] = elig[i] && ka[i] >= thr && !exact[i];
+  } else {
+    const float up = __shfl_up_sync(0xffffffffu, ord_k, 1);
+    const float down = __shfl_down_sync(0xffffffffu, ord_k, 1);
+    const bool amb = lane < n_ord && ((lane > 0 && up - ord_k <= slack) ||
+                                      (lane + 1 < n_ord && ord_k - down <= slack));
+    if (!__any_sync(0xffffffffu, amb)) {
+      // no near-tie among the candidates: the approximate order is the
+      // exact order, and its first k are the selection
+      my_idx = lane < a.k ? ord_e : -1;
+      my_logit = lane < a.k ? ord_l : 0.0f;
+      return;
+    }
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const uint32_t bits = __reduce_or_sync(
+          0xffffffffu,
+          amb && (ord_e >> 5) == i ? (1u << (ord_e & 31)) : 0u);
+      need[i] = ((bits >> lane) & 1u) && !exact[i];
+    }
   }
   exact_sigmoid_keys<NI>(a, lane, lg, need, key);
+  uint32_t code[NI];
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const bool cand = elig[i] && ka[i] >= thr;
@@ -447,7 +525,9 @@ __device__ __forceinline__ void select_token(const RouteSelectArgs& a,
     z = warp_sum(z);
     g = slot ? expf(my_logit - mx) / z : 0.0f;
   } else {
-    const float sg = slot ? sigmoid_score(my_logit) : 0.0f;
+    // gates from the fp32 sigmoid (within 3.5 * 2^-24 of the exact score):
+    // they are compared within a tolerance, unlike the selection keys
+    const float sg = slot ? sigmoid_approx(my_logit) : 0.0f;
     g = sg / warp_sum(sg);
   }
   if (slot) {
@@ -459,7 +539,7 @@ __device__ __forceinline__ void select_token(const RouteSelectArgs& a,
 // One warp per token: the split-K partial sums, added in split order (the
 // loads of one split are independent of each other), then the selection.
 template <int NI>
-__global__ void __launch_bounds__(kSelWarps * 32)
+__global__ void __launch_bounds__(kSelWarps * 32, 4)
     route_select_kernel(RouteSelectArgs a) {
   // keys of each warp's token for the group scan, one pad word per 32 so
   // that lanes reading along different groups hit different banks

@@ -371,6 +371,34 @@ def test_sigmoid_route_near_ties(E, groups, k):
     assert np.abs(gate - rgate).max() <= 2e-6
 
 
+@pytest.mark.parametrize("E,groups,k,dt", [
+    (64, (8, 4, 2), 8, torch.float32), (256, (8, 4, 2), 8, torch.bfloat16),
+    (64, (1, 1, 0), 6, torch.bfloat16), (32, (4, 2, 2), 4, torch.float32)])
+def test_sigmoid_route_paired_ties(E, groups, k, dt):
+    # experts in pairs with the same router row, their biases 0 or 1 ulp of
+    # a key apart: logits spread widely, so few experts are near the k-th
+    # key, but every pair is a near-tie (an exact tie in a third of them)
+    # that the approximate keys cannot order; ids must equal the oracle's
+    # definitional selection bit for bit, ties to the lower index
+    T, D = 300, 64
+    g = torch.Generator().manual_seed(E * 7 + k)
+    x = torch.randn((T, D), generator=g)
+    w = torch.randn((E // 2, D), generator=g) * D ** -0.5
+    w = w.repeat_interleave(2, dim=0)
+    b = (torch.rand(E // 2, generator=g) * 0.2 - 0.1).repeat_interleave(2)
+    step = torch.randint(-1, 2, (E // 2,), generator=g).float()
+    b[1::2] = b[1::2] + step * 2.0 ** -24
+    x = x.to(dt).float()
+    w = w.to(dt).float()
+    idx, gate, logits = run_route(x.to(dt), w.to(dt), None, b, k,
+                                  "sigmoid_bias", groups)
+    assert (logits[:, 0::2] == logits[:, 1::2]).all()   # paired logits
+    ridx, rgate = O.route_from_logits(logits, k, "sigmoid_bias", b.numpy(),
+                                      *groups)
+    assert (idx == ridx).all()
+    assert np.abs(gate - rgate).max() <= 2e-6
+
+
 def test_sigmoid_key_bit_exact():
     # the selection score is an integer decision's input: the device's
     # fp32(sigmoid(l)) must equal the oracle's float64 sigmoid rounded once
