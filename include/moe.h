@@ -84,10 +84,12 @@ typedef enum {
   /* key = logit; gate = softmax over all E experts, taken at the selected
    * ones (the top-1 Switch-style gate). */
   MOE_SCORE_SOFTMAX_FULL = 1,
-  /* s = sigmoid(logit) in fp32, key = s + sel_bias[e] (bias steers
-   * selection only); gate = s_j / sum of the selected s ("Expert
-   * Parallelism in LLMs", Modern Dropless Dynamic Dispatch: bias terms on
-   * routing scores for auxiliary-loss-free balance). */
+  /* s = sigmoid(logit) rounded once to fp32, key = s + sel_bias[e] in
+   * fp32 (bias steers selection only; the selection is exact on these
+   * keys); gate = s_j / sum of the selected s, with s from the fp32
+   * sigmoid there (within 3.5 fp32 ulp) ("Expert Parallelism in LLMs",
+   * Modern Dropless Dynamic Dispatch: bias terms on routing scores for
+   * auxiliary-loss-free balance). */
   MOE_SCORE_SIGMOID_BIAS = 2
 } moe_score;
 
