@@ -243,9 +243,8 @@ def launches_per_step(layer, routed):
         # else the router GEMM and the select kernel
         n += L.moe_route_launches(layer.cfg)
     if not layer.identity:
-        # grouped FFN: bf16 up and down in one tcgen05 launch; fp32 as two
-        # CUDA-core kernels (up, down)
-        n += 1 if layer.dcode == L.MOE_BF16 else 2
+        # grouped FFN: one launch, except fp32 with F > 12288 (up, down)
+        n += 2 if ffn_variant(layer) == 4 else 1
     return n
 
 
@@ -318,7 +317,9 @@ def kernel_label(layer, key):
     from combine_router_gemm_top_b300 import _lib as L
     n_layout = L.moe_dispatch_layout_launches(layer.T, layer.k, layer.E)
     return {
-        "ffn": {1: "moe_grouped_ffn (fp32: up and down kernels on CUDA cores)",
+        "ffn": {1: "moe_grouped_ffn (fp32: one CUDA-core launch, a block "
+                   "per row)",
+                4: "moe_grouped_ffn (fp32: up and down kernels on CUDA cores)",
                 2: "moe_grouped_ffn (one tcgen05 launch, up + down, one SM "
                    "per 128-row tile)",
                 3: "moe_grouped_ffn (one tcgen05 launch, up + down, SM pairs "

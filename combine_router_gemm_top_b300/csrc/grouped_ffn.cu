@@ -121,6 +121,78 @@ __global__ void ffn_down_f32_kernel(int E, int D, int F, int max_rows,
   if (lane < nd) yp[static_cast<int64_t>(row) * D + d0 + lane] = out;
 }
 
+// The same two projections for one row in one block: its H row stays in
+// shared memory (F fp32 values) between them, and each output is formed in
+// the same order as by the two kernels above, so the results are the same
+// bits.  One launch, and H never goes to HBM.
+constexpr int kRowFfnMaxF = 12288;   // 48 KB of H per block
+
+__global__ void __launch_bounds__(256)
+    ffn_row_f32_kernel(int E, int D, int F, int max_rows,
+                       const float* __restrict__ xp,
+                       const int32_t* __restrict__ off,
+                       const float* __restrict__ w13,
+                       const float* __restrict__ w2,
+                       float* __restrict__ yp) {
+  extern __shared__ float hs[];   // [F]
+  const int row = blockIdx.x;
+  const int n_rows = min(__ldg(off + E), max_rows);
+  if (row >= n_rows) return;   // block-uniform
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  const int e = find_expert(off, E, row);
+  const float* x = xp + static_cast<int64_t>(row) * D;
+  for (int f0 = kFpw * warp; f0 < F; f0 += kFpw * nw) {
+    const float* w1 = w13 + (static_cast<int64_t>(e) * 2 * F + f0) * D;
+    const float* w3 = w1 + static_cast<int64_t>(F) * D;
+    const int nf = min(kFpw, F - f0);
+    float g[kFpw], u[kFpw];
+#pragma unroll
+    for (int j = 0; j < kFpw; ++j) g[j] = u[j] = 0.0f;
+    for (int d = lane; d < D; d += 32) {
+      const float xv = __ldg(x + d);
+#pragma unroll
+      for (int j = 0; j < kFpw; ++j) {
+        if (j < nf) {
+          g[j] = fmaf(xv, __ldg(w1 + static_cast<int64_t>(j) * D + d), g[j]);
+          u[j] = fmaf(xv, __ldg(w3 + static_cast<int64_t>(j) * D + d), u[j]);
+        }
+      }
+    }
+    float out = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kFpw; ++j) {
+      const float gs = warp_sum_f32(g[j]);
+      const float us = warp_sum_f32(u[j]);
+      if (lane == j) out = gs / (1.0f + expf(-gs)) * us;
+    }
+    if (lane < nf) hs[f0 + lane] = out;
+  }
+  __syncthreads();
+  for (int d0 = kFpw * warp; d0 < D; d0 += kFpw * nw) {
+    const float* w = w2 + (static_cast<int64_t>(e) * D + d0) * F;
+    const int nd = min(kFpw, D - d0);
+    float acc[kFpw];
+#pragma unroll
+    for (int j = 0; j < kFpw; ++j) acc[j] = 0.0f;
+    for (int f = lane; f < F; f += 32) {
+      const float hv = hs[f];
+#pragma unroll
+      for (int j = 0; j < kFpw; ++j)
+        if (j < nd)
+          acc[j] = fmaf(hv, __ldg(w + static_cast<int64_t>(j) * F + f), acc[j]);
+    }
+    float out = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kFpw; ++j) {
+      const float s = warp_sum_f32(acc[j]);
+      if (lane == j) out = s;
+    }
+    if (lane < nd) yp[static_cast<int64_t>(row) * D + d0 + lane] = out;
+  }
+}
+
 // ----------------------------------------------------------- host
 // Workspace: H [max_rows, F], then (bf16) one ready counter per row block of
 // the fused launch (at most ceil(max_rows / 128) + E blocks) and the SM-pair
@@ -142,7 +214,7 @@ size_t ffn_ws_bytes(int E, int D, int F, int max_rows, int dtype) {
 }
 
 int ffn_variant(int E, int F, int max_rows, int dtype) {
-  if (dtype == MOE_F32) return 1;
+  if (dtype == MOE_F32) return F <= kRowFfnMaxF ? 1 : 4;
   // SM pairs when the experts average at least 1.5 pair row blocks (256
   // rows): below that the 256-row blocks waste more rows than the pairs
   // save
@@ -230,6 +302,14 @@ moe_status launch_grouped_ffn(int E, int D, int F, int max_rows, int dtype,
                               void* ws, int max_ctas, int32_t* status,
                               cudaStream_t stream, int num_sms) {
   if (max_rows == 0) return MOE_OK;
+  if (dtype == MOE_F32 && ffn_variant(E, F, max_rows, dtype) == 1) {
+    ffn_row_f32_kernel<<<static_cast<unsigned>(max_rows), 256,
+                         static_cast<size_t>(F) * sizeof(float), stream>>>(
+        E, D, F, max_rows, static_cast<const float*>(xp), offsets,
+        static_cast<const float*>(w13), static_cast<const float*>(w2),
+        static_cast<float*>(yp));
+    return launch_status();
+  }
   if (dtype == MOE_F32) {
     float* h = static_cast<float*>(ws);
     // one warp per row and kFpw outputs, 8 warps a block

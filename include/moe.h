@@ -249,7 +249,9 @@ MOE_API size_t moe_grouped_ffn_workspace_size(int32_t E, int32_t D, int32_t F,
                                       int32_t max_rows, int32_t dtype);
 
 /* moe_grouped_ffn_variant -- which implementation moe_grouped_ffn runs for
- * this size: 1 = fp32 FMA kernels (MOE_F32, two launches); 2 = one
+ * this size: 1 = fp32 FMA kernel, one launch of one block per row with its
+ * H row in shared memory (MOE_F32, F <= 12288); 4 = fp32 FMA kernels, up
+ * then down (MOE_F32, F > 12288, two launches); 2 = one
  * persistent tcgen05 launch with a 128-row tile on each SM (cooperative);
  * 3 = one persistent tcgen05 launch of SM pairs (2-CTA clusters,
  * cta_group::2) with 256-row tiles claimed in order, taken when the experts

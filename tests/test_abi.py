@@ -142,8 +142,9 @@ def test_layout_launches(lib):
 
 
 def test_grouped_ffn_variant(lib):
-    # 1: fp32 FMA; 2: one SM per 128-row tile; 3: SM pairs, taken for
-    # F % 256 == 0, E <= 256 and max_rows >= 384 E; 0: rejected or empty
+    # 1: fp32 FMA, one block per row (F <= 12288); 4: fp32 FMA, up then
+    # down; 2: one SM per 128-row tile; 3: SM pairs, taken for F % 256 == 0,
+    # E <= 256 and max_rows >= 384 E; 0: rejected or empty
     bf, f32 = L.MOE_BF16, L.MOE_F32
     for args, v in [((8, 4096, 14336, 4096, bf), 3),     # Mixtral-like
                     ((8, 4096, 14336, 3071, bf), 2),
@@ -156,6 +157,8 @@ def test_grouped_ffn_variant(lib):
                     ((257, 256, 256, 1 << 20, bf), 2),   # E > 256
                     ((64, 1024, 4096, 16384, bf), 2),    # Switch-like
                     ((8, 64, 128, 4096, f32), 1),
+                    ((8, 64, 12288, 4096, f32), 1),
+                    ((8, 64, 12289, 4096, f32), 4),
                     ((8, 4096, 14336, 0, bf), 0),
                     ((8, 4000, 14336, 4096, bf), 0),     # D % 64 != 0
                     ((0, 4096, 14336, 4096, bf), 0)]:

@@ -496,8 +496,10 @@ FFN_CASES = [
     (5, 192, 256, [7, 0, 0, 130, 64], torch.bfloat16),
     (8, 1024, 512, [100, 300, 0, 17, 128, 129, 255, 1], torch.bfloat16),
     (8, 64, 128, [10, 50, 0, 3, 128, 70, 1, 250], torch.float32),
-    # fp32 with D and F not multiples of a warp's 32 lanes
+    # fp32 with D and F not multiples of a warp's 32 lanes (one block per
+    # row), and F past the shared-memory row buffer (up, then down)
     (3, 36, 100, [5, 40, 33], torch.float32),
+    (2, 40, 12300, [7, 20], torch.float32),
     # tails of every swapped MMA width (16..112) and the 112/113 switch to
     # the normal tile; D = 320 leaves a down-projection tile half outside D
     (8, 256, 256, [16, 33, 112, 113, 128 + 48, 256 + 97, 240, 2],
