@@ -118,7 +118,8 @@ size_t moe_route_workspace_size(const moe_route_cfg* cfg) {
 
 int32_t moe_route_launches(const moe_route_cfg* cfg) {
   if (!route_cfg_ok(cfg) || cfg->T == 0) return 0;
-  return route_single_kernel(*cfg, num_sms()) ? 1 : 2;
+  const int sms = num_sms();
+  return route_single_kernel(*cfg, sms) || route_fused_gemm(*cfg, sms) ? 1 : 2;
 }
 
 moe_status moe_route(const moe_route_cfg* cfg, const void* x, const void* w_r,

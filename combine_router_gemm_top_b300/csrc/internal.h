@@ -30,6 +30,7 @@ struct RoutePlan {
 };
 RoutePlan plan_route(const moe_route_cfg& c, int num_sms);
 bool route_single_kernel(const moe_route_cfg& c, int num_sms);
+bool route_fused_gemm(const moe_route_cfg& c, int num_sms);
 
 struct RouteSelectArgs {
   int T, E, k, score, n_groups, topk_groups, group_score_topk, splits;

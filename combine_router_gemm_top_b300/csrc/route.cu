@@ -828,6 +828,17 @@ RoutePlan plan_route(const moe_route_cfg& c, int num_sms) {
 // cores in bf16), then the select kernel.
 constexpr int kWarpRouteSmem = 96 * 1024;
 static int route_ep(int E) { return E <= 8 ? 8 : E <= 16 ? 16 : 32; }
+// The router GEMM selects in its epilogue (no partial logits, no select
+// launch) when one thread can do a token's whole selection from registers:
+// bf16, one K split, a softmax score without groups, k <= 2 and E <= 64.
+bool route_fused_gemm(const moe_route_cfg& c, int num_sms) {
+  if (route_single_kernel(c, num_sms) || c.dtype != MOE_BF16) return false;
+  if (c.score == MOE_SCORE_SIGMOID_BIAS || c.n_groups != 1 || c.k > 2 ||
+      c.E > kRouteSelMaxE)
+    return false;
+  return plan_route(c, num_sms).splits == 1;
+}
+
 bool route_single_kernel(const moe_route_cfg& c, int num_sms) {
   if (c.E > 32) return false;
   const bool small_w = static_cast<int64_t>(route_ep(c.E)) * c.D *
@@ -936,6 +947,15 @@ moe_status launch_route(const moe_route_cfg& c, const void* x, const void* w_r,
     g.out_cols = c.E;
     g.status = status;
     g.wait_limit_ns = kWaitLimitNs;
+    const bool fused = route_fused_gemm(c, num_sms);
+    if (fused) {
+      g.sel_idx = topk_idx;
+      g.sel_gate = topk_gate;
+      g.sel_logits = logits_out;
+      g.sel_offset = logit_offset;
+      g.sel_k = c.k;
+      g.sel_full = c.score == MOE_SCORE_SOFTMAX_FULL ? 1 : 0;
+    }
     const size_t smem = umma_gemm_smem_bytes(g.BN, g.stages);
     static std::atomic<uint64_t> attr_done{0};
     if (!set_smem_limit_once(
@@ -945,6 +965,7 @@ moe_status launch_route(const moe_route_cfg& c, const void* x, const void* w_r,
     const int tiles = static_cast<int>(ceil_div(c.T, kBM)) * p.splits;
     const int grid = tiles < num_sms ? tiles : num_sms;
     umma_gemm_kernel<kRoute><<<grid, kGemmThreads, smem, stream>>>(tmA, tmB, g);
+    if (fused) return launch_status();
   } else {
     const int64_t n = static_cast<int64_t>(c.T) * c.E;
     route_gemm_f32_kernel<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0,

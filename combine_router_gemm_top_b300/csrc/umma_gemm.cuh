@@ -19,7 +19,8 @@
 // Three modes share the pipeline and differ in tile scheduling, the B
 // operand rows and the epilogue:
 //   kRoute  router logits, split-K: tile = (m block, K split); writes fp32
-//           partial logits [split][T][E].
+//           partial logits [split][T][E], or with one split and a softmax
+//           top-1/top-2 of at most 64 experts selects in the epilogue.
 //   kUp     grouped SwiGLU up-projection: tile = (expert, n block, m block)
 //           over ragged expert segments; B = 128 gate rows of W1 stacked on
 //           the matching 128 up rows of W3 (BN = 256), epilogue
@@ -110,6 +111,9 @@ constexpr uint32_t kATileBytes = kBM * kBK * 2;
 constexpr int kStageLd = 36;
 constexpr size_t kStageBytes = static_cast<size_t>(kEpiWarps) * 32 * kStageLd * 4;
 
+// experts the router GEMM's epilogue selection holds in registers
+constexpr int kRouteSelMaxE = 64;
+
 struct GemmArgs {
   int32_t M;                // route: T ; grouped: rows allocated (max_rows)
   int32_t k_blocks;         // K / 64 (rounded up)
@@ -140,6 +144,14 @@ struct GemmArgs {
   // router backward
   int32_t row_limit;        // kRDW: output rows (E); 0 = no row mask
   int64_t split_stride;     // kRDW: elements between split partials
+  // kRoute with one K split, softmax scores, no groups, k <= 2: the epilogue
+  // selects (sel_idx != nullptr) instead of writing partial logits
+  int32_t* sel_idx;         // [T, k] out
+  float* sel_gate;          // [T, k] out
+  float* sel_logits;        // [T, E] out or nullptr
+  const float* sel_offset;  // [E] or nullptr, added to the logits
+  int32_t sel_k;            // 1 or 2
+  int32_t sel_full;         // 1: softmax over all E (else over the k)
 };
 
 struct TileInfo {
@@ -342,6 +354,84 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
   }
   const int64_t grow = static_cast<int64_t>(ti.a_row) + r;
   const bool valid = r < ti.rows && grow >= 0 && grow < a.M;
+  if (MODE == kRoute && a.sel_idx != nullptr) {
+    // one thread per token row selects over its E (<= 64) logits, held in
+    // registers: the top two in expert order (a strictly larger key
+    // replaces, so ties keep the lower index), then the softmax terms, which
+    // are independent of each other once the maximum (the top key) is known
+    if (half != 0) return;
+    const int E = a.E;
+    float v[kRouteSelMaxE];
+#pragma unroll
+    for (int c = 0; c < kRouteSelMaxE; c += 16) {
+      if (c < a.BN) {
+        float t[16];
+        tmem_ld16(tmem_row + c, t);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[c + i] = t[i];
+      }
+    }
+    if (!valid) return;
+#pragma unroll
+    for (int e = 0; e < kRouteSelMaxE; ++e)
+      if (e < E && a.sel_offset != nullptr)
+        v[e] = __fadd_rn(v[e], __ldg(a.sel_offset + e));
+    float b0 = -INFINITY, b1 = -INFINITY;
+    int i0 = -1, i1 = -1;
+#pragma unroll
+    for (int e = 0; e < kRouteSelMaxE; ++e) {
+      if (e < E) {
+        const float l = v[e];
+        if (l > b0) {
+          b1 = b0;
+          i1 = i0;
+          b0 = l;
+          i0 = e;
+        } else if (l > b1) {
+          b1 = l;
+          i1 = e;
+        }
+      }
+    }
+    if (a.sel_logits != nullptr) {
+      float* lout = a.sel_logits + grow * E;
+      if ((E & 3) == 0) {
+#pragma unroll
+        for (int e = 0; e < kRouteSelMaxE; e += 4)
+          if (e < E)
+            *reinterpret_cast<float4*>(lout + e) =
+                make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kRouteSelMaxE; ++e)
+          if (e < E) lout[e] = v[e];
+      }
+    }
+    float g0, g1 = 0.0f;
+    if (a.sel_full) {
+      float zs[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int e = 0; e < kRouteSelMaxE; ++e)
+        if (e < E) zs[e & 3] += expf(v[e] - b0);
+      const float z = (zs[0] + zs[1]) + (zs[2] + zs[3]);
+      g0 = 1.0f / z;
+      if (a.sel_k > 1) g1 = expf(b1 - b0) / z;
+    } else if (a.sel_k > 1) {
+      const float e1 = expf(b1 - b0);
+      const float zz = 1.0f + e1;
+      g0 = 1.0f / zz;
+      g1 = e1 / zz;
+    } else {
+      g0 = 1.0f;
+    }
+    a.sel_idx[grow * a.sel_k] = i0;
+    a.sel_gate[grow * a.sel_k] = g0;
+    if (a.sel_k > 1) {
+      a.sel_idx[grow * a.sel_k + 1] = i1;
+      a.sel_gate[grow * a.sel_k + 1] = g1;
+    }
+    return;
+  }
   if (MODE == kRoute) {
     // partial logits [split][T][E] fp32
     float* out = reinterpret_cast<float*>(a.out) +

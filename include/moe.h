@@ -125,8 +125,11 @@ MOE_API size_t moe_route_workspace_size(const moe_route_cfg* cfg);
  *   fp32: W_r padded to 8, 16 or 32 rows takes at most 96 KiB (one warp per
  *         token computes the logits on the CUDA cores from W_r in shared
  *         memory and selects);
- * else 2 (the router GEMM, then the select kernel); 0 for an invalid cfg or
- * T = 0.  Host only. */
+ * also 1 in bf16 for E <= 64 with a softmax score, no groups and k <= 2
+ * when the router GEMM runs as one K split (T past about 74 row blocks of
+ * 128 per 148 SMs, or D < 256): it selects in its epilogue; else 2 (the
+ * router GEMM, then the select kernel); 0 for an invalid cfg or T = 0.
+ * Host only. */
 MOE_API int32_t moe_route_launches(const moe_route_cfg* cfg);
 
 /* moe_route -- router GEMM, score, top-k and gates

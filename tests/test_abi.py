@@ -110,20 +110,36 @@ def test_layout_rejects_bad_sizes(lib):
 def test_route_launches(lib):
     # one kernel up to 32 experts: in bf16 (the MMA router) for E <= 8, a
     # padded W_r of <= 96 KiB, or T <= 16 tokens per SM; in fp32 for a
-    # padded W_r of <= 96 KiB (in shared memory); else GEMM + select
+    # padded W_r of <= 96 KiB (in shared memory); the bf16 router GEMM alone
+    # when it selects in its epilogue (one K split, softmax, no groups,
+    # k <= 2, E <= 64); else GEMM + select
     for E, D, dt, n in [(8, 4096, L.MOE_BF16, 1), (32, 1024, L.MOE_BF16, 1),
                         (32, 4096, L.MOE_BF16, 1), (8, 65536, L.MOE_BF16, 1),
-                        (33, 64, L.MOE_BF16, 2), (256, 4096, L.MOE_BF16, 2),
+                        (33, 64, L.MOE_BF16, 1), (64, 4096, L.MOE_BF16, 2),
+                        (256, 4096, L.MOE_BF16, 2),
                         (8, 3072, L.MOE_F32, 1), (8, 4096, L.MOE_F32, 2),
                         (32, 1024, L.MOE_F32, 2)]:
         cfg = L.route_cfg(2048, D, E, 2, dt, 0)
         assert lib.moe_route_launches(ctypes.byref(cfg)) == n, (E, D, dt)
     # above one 16-token tile per SM, bf16 W_r over 96 KiB with more than 8
     # experts goes back to the GEMM (148 SMs without a device)
-    for T, E, D, n in [(16384, 32, 4096, 2), (16384, 16, 4096, 2),
+    for T, E, D, n in [(16384, 32, 4096, 1), (16384, 16, 4096, 1),
                        (16384, 8, 4096, 1), (16384, 32, 1024, 1)]:
         cfg = L.route_cfg(T, D, E, 2, L.MOE_BF16, 0)
         assert lib.moe_route_launches(ctypes.byref(cfg)) == n, (T, E, D)
+    # the fused GEMM: one K split at the Switch-like shape; not with the
+    # sigmoid score, groups, k > 2, E > 64 or several K splits
+    for (T, D, E, k, score, groups), n in [
+            ((16384, 1024, 64, 1, 1, (1, 1, 0)), 1),
+            ((16384, 1024, 40, 2, 0, (1, 1, 0)), 1),
+            ((16384, 1024, 65, 1, 0, (1, 1, 0)), 2),
+            ((16384, 1024, 64, 1, 2, (1, 1, 0)), 2),
+            ((16384, 1024, 64, 2, 0, (4, 2, 2)), 2),
+            ((16384, 1024, 64, 3, 0, (1, 1, 0)), 2),
+            ((16384, 1024, 144, 1, 0, (1, 1, 0)), 2),
+            ((2048, 1024, 64, 1, 1, (1, 1, 0)), 2)]:
+        cfg = L.route_cfg(T, D, E, k, L.MOE_BF16, score, *groups)
+        assert lib.moe_route_launches(ctypes.byref(cfg)) == n, (T, D, E, k)
     assert lib.moe_route_launches(ctypes.byref(
         L.route_cfg(0, 4096, 8, 2, L.MOE_BF16, 0))) == 0
     assert lib.moe_route_launches(ctypes.byref(

@@ -284,6 +284,14 @@ ROUTE_CASES = [
     # fits one 16-token tile per SM, the router GEMM (16 columns) above that
     (2300, 4096, 32, 4, torch.bfloat16, "softmax_full", (1, 1, 0), None, 1.5, None),
     (3000, 4096, 16, 4, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
+    # the router GEMM selecting in its epilogue (one K split, softmax, k <=
+    # 2, E <= 64): the Switch-like shape, 60 experts (a ragged last column
+    # chunk), 40 and 33 experts; then 100 experts, past it
+    (16384, 1024, 64, 1, torch.bfloat16, "softmax_full", (1, 1, 0), None, 1.5, None),
+    (10000, 256, 60, 2, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
+    (12000, 512, 40, 2, torch.bfloat16, "softmax_full", (1, 1, 0), None, None, None),
+    (10500, 128, 33, 1, torch.bfloat16, "softmax_topk", (1, 1, 0), None, 0.5, None),
+    (10000, 256, 100, 2, torch.bfloat16, "softmax_topk", (1, 1, 0), None, None, None),
 ]
 
 
@@ -312,11 +320,12 @@ def test_route_logits_independent_of_batch_size(E, D, dt):
     assert np.array_equal(big[-37:].view(np.int32), tail.view(np.int32))
 
 
-@pytest.mark.parametrize("T", [512, 10240])
-def test_route_ties_go_to_lower_index(T):
+@pytest.mark.parametrize("T,E,k", [(512, 16, 4), (10240, 16, 4),
+                                   (10240, 64, 2), (10240, 64, 1)])
+def test_route_ties_go_to_lower_index(T, E, k):
     # D = E and w_r = identity: logits equal x exactly (small integers in
-    # bf16), so many experts tie; the lower index must win every tie
-    E, k = 16, 4
+    # bf16), so many experts tie; the lower index must win every tie (64
+    # experts at T = 10240: the router GEMM selecting in its epilogue)
     rng = np.random.default_rng(3)
     xl = rng.integers(-2, 3, size=(T, E)).astype(np.float32)
     x = torch.tensor(xl).to(torch.bfloat16)
