@@ -126,10 +126,11 @@ MOE_API size_t moe_route_workspace_size(const moe_route_cfg* cfg);
  *         token computes the logits on the CUDA cores from W_r in shared
  *         memory and selects);
  * also 1 in bf16 for E <= 64 with a softmax score, no groups and k <= 2
- * when the router GEMM runs as one K split (T past about 74 row blocks of
- * 128 per 148 SMs, or D < 256): it selects in its epilogue; else 2 (the
- * router GEMM, then the select kernel); 0 for an invalid cfg or T = 0.
- * Host only. */
+ * when the router GEMM runs as one K split (moe_route_workspace_size is
+ * then T * E * 4 bytes; it splits K while its 128-token row blocks are
+ * fewer than half the SMs): it selects in its epilogue; else 2 (the router
+ * GEMM, then the select kernel); 0 for an invalid cfg or T = 0.  Host
+ * only. */
 MOE_API int32_t moe_route_launches(const moe_route_cfg* cfg);
 
 /* moe_route -- router GEMM, score, top-k and gates
