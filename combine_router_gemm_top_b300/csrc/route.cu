@@ -201,6 +201,69 @@ __device__ __forceinline__ void topk_rounds(uint32_t (&code)[NI],
   }
 }
 
+// The same top-k as topk_rounds with each lane's NI candidates sorted
+// first (key code descending, the lower expert first on equal codes), so a
+// round compares one head per lane: the largest head code, the lowest
+// expert holding it, and the winner's lane drops its head.  The lowest
+// expert with the top code is always a head (a lane's own equal codes are
+// ordered by expert), so the rounds pick what topk_rounds picks.
+template <int NI>
+__device__ __forceinline__ void topk_presorted(uint32_t (&code)[NI],
+                                               const float (&lg)[NI], int k,
+                                               int lane, int& my_idx,
+                                               float& my_logit) {
+  int ex[NI];
+  float lv[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    ex[i] = lane + 32 * i;
+    lv[i] = lg[i];
+  }
+  // odd-even transposition sort, descending by (code, -expert)
+#pragma unroll
+  for (int pass = 0; pass < NI; ++pass) {
+#pragma unroll
+    for (int i = pass & 1; i + 1 < NI; i += 2) {
+      const bool sw = code[i + 1] > code[i] ||
+                      (code[i + 1] == code[i] && ex[i + 1] < ex[i]);
+      if (sw) {
+        const uint32_t tc = code[i];
+        code[i] = code[i + 1];
+        code[i + 1] = tc;
+        const int te = ex[i];
+        ex[i] = ex[i + 1];
+        ex[i + 1] = te;
+        const float tl = lv[i];
+        lv[i] = lv[i + 1];
+        lv[i + 1] = tl;
+      }
+    }
+  }
+  my_idx = -1;
+  my_logit = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const uint32_t top = __reduce_max_sync(0xffffffffu, code[0]);
+    if (top == 0) break;   // no eligible expert left
+    const uint32_t cand = code[0] == top ? static_cast<uint32_t>(ex[0])
+                                         : 0xffffffffu;
+    const int w = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
+    const float wl = __shfl_sync(0xffffffffu, lv[0], w & 31);
+    if (lane == j) {
+      my_idx = w;
+      my_logit = wl;
+    }
+    if ((w & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i + 1 < NI; ++i) {
+        code[i] = code[i + 1];
+        ex[i] = ex[i + 1];
+        lv[i] = lv[i + 1];
+      }
+      code[NI - 1] = 0u;
+    }
+  }
+}
+
 // Softmax modes: the key is the logit itself.
 template <int NI>
 __device__ __forceinline__ void select_by_logit(const RouteSelectArgs& a,
@@ -233,7 +296,7 @@ __device__ __forceinline__ void select_by_logit(const RouteSelectArgs& a,
       if (e < E && !((chosen >> group_of(e, inv_gs)) & 1u)) code[i] = 0u;
     }
   }
-  topk_rounds<NI>(code, lg, a.k, lane, my_idx, my_logit);
+  topk_presorted<NI>(code, lg, a.k, lane, my_idx, my_logit);
 }
 
 // fp32 approximation of the sigmoid score: expf (within 2 ulp), one add and
@@ -991,6 +1054,7 @@ moe_status launch_route(const moe_route_cfg& c, const void* x, const void* w_r,
   s.topk_gate = topk_gate;
   s.logits_out = logits_out;
   const int warps = kSelWarps;
+  // four blocks per SM stay resident; past that the warps stride
   const unsigned grid = static_cast<unsigned>(ceil_div(c.T, warps));
   const int ni = static_cast<int>(ceil_div(c.E, 32));
   if (ni <= 1)
