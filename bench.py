@@ -137,9 +137,9 @@ K_graph_cap = 200
 #   Mixtral-like   3.5955 GB read + 187.4 MB written (SM pairs)
 #   DeepSeek-like 23.3931 GB read + 598.7 MB written (one SM per tile)
 #   Switch-like    522.6 MB read +  17.4 MB written (one SM per tile)
-NCU_DRAM_BYTES = {("mixtral_bf16", 2048, 8, "ffn", 3): 3.7829e9,
-                  ("deepseek_bf16", 4096, 256, "ffn", 2): 2.39918e10,
-                  ("switch_bf16", 16384, 64, "ffn", 2): 5.400e8}
+NCU_DRAM_BYTES = {("mixtral_bf16", 2048, 8, "ffn", 3): 3.3364e9,
+                  ("deepseek_bf16", 4096, 256, "ffn", 2): 2.39966e10,
+                  ("switch_bf16", 16384, 64, "ffn", 2): 5.3954e8}
 
 # tokens of the bounded CPU-oracle sample, per workload (about 10-30 s of
 # host work)
