@@ -722,9 +722,11 @@ __global__ void __launch_bounds__(kSelWarps * 32)
 }
 
 // The bf16 router for up to 32 experts in one kernel, on the warp-level MMA.
-// A block takes 16 tokens and its 16 warps split D between them; each warp
-// accumulates a 16-token x EP-expert tile with m16n8k16 MMAs whose operands
-// come straight from global memory into registers.  A dot product may take
+// A block takes tb tokens (16, or fewer when 16 would leave SMs without a
+// block; the MMA tile's other rows load nothing) and its 16 warps split D
+// between them; each warp accumulates a 16-token x EP-expert tile with
+// m16n8k16 MMAs in two chains (even and odd chunks), operands straight from
+// global memory into registers, one batch of loads per warp at D = 4096.  A dot product may take
 // its D terms in any order, so lane (g, t) loads the 16 bytes at elements
 // 8t..8t+7 of each 32-element chunk of token rows g and g + 8 and of expert
 // row g, and hands elements 8t..8t+3 to one MMA and 8t+4..8t+7 to a second
