@@ -1022,10 +1022,12 @@ moe_status launch_route(const moe_route_cfg& c, const void* x, const void* w_r,
       g.sel_full = c.score == MOE_SCORE_SOFTMAX_FULL ? 1 : 0;
     }
     const size_t smem = umma_gemm_smem_bytes(g.BN, g.stages);
+    // the kernel's static shared memory (the epilogue selection's exchange
+    // slots, 6 KB) comes out of the same 227 KB as the dynamic part
     static std::atomic<uint64_t> attr_done{0};
     if (!set_smem_limit_once(
             reinterpret_cast<const void*>(umma_gemm_kernel<kRoute>),
-            227 * 1024, &attr_done))
+            (227 - 8) * 1024, &attr_done))
       return MOE_ERR_CUDA;
     const int tiles = static_cast<int>(ceil_div(c.T, kBM)) * p.splits;
     const int grid = tiles < num_sms ? tiles : num_sms;

@@ -171,6 +171,7 @@ struct GemmShared {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t xfull[2][4];   // route selection: half 1 -> half 0, per quarter
   uint32_t tmem_base;
   int32_t abort;
   int32_t total_tiles;
@@ -277,10 +278,10 @@ __device__ __forceinline__ float silu_f32(float g) {
 // Epilogue of one tile for the thread owning tile row `r` (TMEM lane r);
 // `half` selects the alternate column chunks this warp handles.
 template <int MODE>
-__device__ __forceinline__ void epilogue_row(const GemmArgs& a,
-                                             const TileInfo& ti,
-                                             uint32_t tmem_row, int r,
-                                             int half, float* stage) {
+__device__ __forceinline__ void epilogue_row(
+    const GemmArgs& a, const TileInfo& ti, uint32_t tmem_row, int r, int half,
+    float* stage, int parity = 0, uint64_t* xbar = nullptr,
+    uint32_t xphase = 0, volatile int* abort_flag = nullptr) {
   if (MODE != kRoute && ti.swap_n != 0) {
     // swapped tail: TMEM lane r is output feature out_col + r (and, for the
     // down projection, out_col + 128 + r); column j is token row a_row + j
@@ -355,79 +356,135 @@ __device__ __forceinline__ void epilogue_row(const GemmArgs& a,
   const int64_t grow = static_cast<int64_t>(ti.a_row) + r;
   const bool valid = r < ti.rows && grow >= 0 && grow < a.M;
   if (MODE == kRoute && a.sel_idx != nullptr) {
-    // one thread per token row selects over its E (<= 64) logits, held in
-    // registers: the top two in expert order (a strictly larger key
-    // replaces, so ties keep the lower index), then the softmax terms, which
-    // are independent of each other once the maximum (the top key) is known
-    if (half != 0) return;
+    // The two epilogue warps on a token row's TMEM lanes share its E (<= 64)
+    // logits: half 0 the first ceil(n/2) 16-column chunks, half 1 the rest,
+    // each in registers.  Each keeps its top two in expert order (a
+    // strictly larger key replaces, so ties keep the lower index) and, for
+    // the full softmax, its maximum and the sum of its terms, independent of
+    // each other once that maximum is known.  Half 1 hands its part to half
+    // 0 through shared memory and an mbarrier per quarter (bounded wait),
+    // and half 0 merges, half 1's experts losing ties.  Slots alternate with
+    // the accumulator: half 1 rewrites one only for the tile after next,
+    // whose accumulator half 0 must first have released.
+    __shared__ float xk[2][4][32][4];
+    __shared__ int xi[2][4][32][2];
+    constexpr int kHalfE = kRouteSelMaxE / 2;
     const int E = a.E;
-    float v[kRouteSelMaxE];
+    const int quarter = r >> 5;
+    const int lane = r & 31;
+    const int nch = a.BN / 16;
+    const int c_lo = half == 0 ? 0 : 16 * ((nch + 1) / 2);
+    const int c_hi = half == 0 ? 16 * ((nch + 1) / 2) : a.BN;
+    float v[kHalfE];
 #pragma unroll
-    for (int c = 0; c < kRouteSelMaxE; c += 16) {
-      if (c < a.BN) {
+    for (int c = 0; c < kHalfE; c += 16) {
+      if (c_lo + c < c_hi) {
         float t[16];
-        tmem_ld16(tmem_row + c, t);
+        tmem_ld16(tmem_row + c_lo + c, t);
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[c + i] = t[i];
       }
     }
-    if (!valid) return;
-#pragma unroll
-    for (int e = 0; e < kRouteSelMaxE; ++e)
-      if (e < E && a.sel_offset != nullptr)
-        v[e] = __fadd_rn(v[e], __ldg(a.sel_offset + e));
-    float b0 = -INFINITY, b1 = -INFINITY;
+    float b0 = -INFINITY, b1 = -INFINITY, z = 0.0f;
     int i0 = -1, i1 = -1;
+    if (valid) {
 #pragma unroll
-    for (int e = 0; e < kRouteSelMaxE; ++e) {
-      if (e < E) {
-        const float l = v[e];
-        if (l > b0) {
-          b1 = b0;
-          i1 = i0;
-          b0 = l;
-          i0 = e;
-        } else if (l > b1) {
-          b1 = l;
-          i1 = e;
+      for (int c = 0; c < kHalfE; ++c) {
+        const int e = c_lo + c;
+        if (e < c_hi && e < E) {
+          float l = v[c];
+          if (a.sel_offset != nullptr) l = __fadd_rn(l, __ldg(a.sel_offset + e));
+          v[c] = l;
+          if (l > b0) {
+            b1 = b0;
+            i1 = i0;
+            b0 = l;
+            i0 = e;
+          } else if (l > b1) {
+            b1 = l;
+            i1 = e;
+          }
         }
       }
+      if (a.sel_logits != nullptr) {
+        float* lout = a.sel_logits + grow * E;
+#pragma unroll
+        for (int c = 0; c < kHalfE; ++c)
+          if (c_lo + c < c_hi && c_lo + c < E) lout[c_lo + c] = v[c];
+      }
+      if (a.sel_full && i0 >= 0) {
+        float zs[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int c = 0; c < kHalfE; ++c)
+          if (c_lo + c < c_hi && c_lo + c < E) zs[c & 3] += expf(v[c] - b0);
+        z = (zs[0] + zs[1]) + (zs[2] + zs[3]);
+      }
     }
-    if (a.sel_logits != nullptr) {
-      float* lout = a.sel_logits + grow * E;
-      if ((E & 3) == 0) {
-#pragma unroll
-        for (int e = 0; e < kRouteSelMaxE; e += 4)
-          if (e < E)
-            *reinterpret_cast<float4*>(lout + e) =
-                make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+    const int slot = parity & 1;
+    uint64_t* bar = xbar + 4 * slot + quarter;
+    if (half == 1) {
+      xk[slot][quarter][lane][0] = b0;
+      xk[slot][quarter][lane][1] = b1;
+      xk[slot][quarter][lane][2] = z;
+      xi[slot][quarter][lane][0] = i0;
+      xi[slot][quarter][lane][1] = i1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+      return;
+    }
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait(bar, xphase, abort_flag, a.wait_limit_ns);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    if (!ok || !valid) return;
+    const float c0 = xk[slot][quarter][lane][0];
+    const float c1 = xk[slot][quarter][lane][1];
+    const float zc = xk[slot][quarter][lane][2];
+    const int j0 = xi[slot][quarter][lane][0];
+    const int j1 = xi[slot][quarter][lane][1];
+    float m0, m1;
+    int k0, k1;
+    if (c0 > b0) {
+      m0 = c0;
+      k0 = j0;
+      if (c1 > b0) {
+        m1 = c1;
+        k1 = j1;
       } else {
-#pragma unroll
-        for (int e = 0; e < kRouteSelMaxE; ++e)
-          if (e < E) lout[e] = v[e];
+        m1 = b0;
+        k1 = i0;
+      }
+    } else {
+      m0 = b0;
+      k0 = i0;
+      if (c0 > b1) {
+        m1 = c0;
+        k1 = j0;
+      } else {
+        m1 = b1;
+        k1 = i1;
       }
     }
     float g0, g1 = 0.0f;
     if (a.sel_full) {
-      float zs[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-      for (int e = 0; e < kRouteSelMaxE; ++e)
-        if (e < E) zs[e & 3] += expf(v[e] - b0);
-      const float z = (zs[0] + zs[1]) + (zs[2] + zs[3]);
-      g0 = 1.0f / z;
-      if (a.sel_k > 1) g1 = expf(b1 - b0) / z;
+      // each half's sum is over its own maximum; m0 is the overall one
+      float zt = 0.0f;
+      if (i0 >= 0) zt += z * expf(b0 - m0);
+      if (j0 >= 0) zt += zc * expf(c0 - m0);
+      g0 = 1.0f / zt;
+      if (a.sel_k > 1) g1 = expf(m1 - m0) / zt;
     } else if (a.sel_k > 1) {
-      const float e1 = expf(b1 - b0);
+      const float e1 = expf(m1 - m0);
       const float zz = 1.0f + e1;
       g0 = 1.0f / zz;
       g1 = e1 / zz;
     } else {
       g0 = 1.0f;
     }
-    a.sel_idx[grow * a.sel_k] = i0;
+    a.sel_idx[grow * a.sel_k] = k0;
     a.sel_gate[grow * a.sel_k] = g0;
     if (a.sel_k > 1) {
-      a.sel_idx[grow * a.sel_k + 1] = i1;
+      a.sel_idx[grow * a.sel_k + 1] = k1;
       a.sel_gate[grow * a.sel_k + 1] = g1;
     }
     return;
@@ -580,6 +637,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.tfull[i], 1);
       mbar_init(&sh.tempty[i], kEpiWarps);
+      for (int q = 0; q < 4; ++q) mbar_init(&sh.xfull[i][q], 1);
     }
     mbar_init(&sh.drain, 1);
     sh.abort = 0;
@@ -809,7 +867,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t tmem_row =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
           acc * a.BN;
-      epilogue_row<MODE>(a, ti, tmem_row, r, half, stage);
+      epilogue_row<MODE>(a, ti, tmem_row, r, half, stage, acc,
+                         &sh.xfull[0][0], acc_phase, abort_flag);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.tempty[acc]);
