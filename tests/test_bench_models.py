@@ -70,6 +70,18 @@ def test_permute_reads_only_tokens_with_a_kept_pair(bench):
     assert dropless["permute"]["bytes"] == (wl.T + n) * wl.D * 2 + ids
 
 
+def test_tokens_kept_counts_tokens_with_a_kept_pair(bench):
+    # dst_row < 0 marks a dropped pair; a token counts once if any of its k
+    # pairs was kept
+    import torch
+
+    class FakeLayer:
+        T, k = 4, 2
+        dst_row = torch.tensor([0, -1, -1, -1, 3, 4, -1, 7, 99, 99],
+                               dtype=torch.int32)   # padded past T*k
+    assert bench.tokens_kept(FakeLayer()) == 3
+
+
 def test_sweep_permute_and_combine_bytes(bench):
     wl = W.WORKLOADS["sweep_bf16_uniform_T65536"]
     n = wl.T * wl.k
