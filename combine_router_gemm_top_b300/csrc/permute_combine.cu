@@ -47,11 +47,15 @@ __global__ void __launch_bounds__(kRowWarps * 32)
     // a token with no kept slot (all dropped at capacity) is not read
     if (!__any_sync(0xffffffffu, my_dst >= 0)) continue;
     const uint4* src = x + t * nvec;
-    for (int v0 = v_begin + lane; v0 < v_end; v0 += 32 * kUnroll) {
+    // The step loop is warp-uniform (every lane runs every step, out-of-range
+    // vectors masked) so that the full-mask shuffle below always has all 32
+    // lanes: with a lane-strided bound, a segment shorter than 32 vectors, or
+    // one whose length is 1-31 past a multiple of 128, would leave lanes out.
+    for (int v0 = v_begin; v0 < v_end; v0 += 32 * kUnroll) {
       uint4 buf[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int v = v0 + u * 32;
+        const int v = v0 + lane + u * 32;
         if (v < v_end) buf[u] = ld_nc_v4(src + v);
       }
       for (int j = 0; j < k; ++j) {
@@ -60,7 +64,7 @@ __global__ void __launch_bounds__(kRowWarps * 32)
         uint4* dst = xp + static_cast<int64_t>(r) * nvec;
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-          const int v = v0 + u * 32;
+          const int v = v0 + lane + u * 32;
           if (v < v_end) st_v4(dst + v, buf[u]);
         }
       }
@@ -94,7 +98,9 @@ __global__ void __launch_bounds__(kRowWarps * 32)
         lane < k ? (gate != nullptr ? __ldg(gate + t * k + lane) : 1.0f)
                  : 0.0f;
     uint4* out = y + t * nvec;
-    for (int v0 = v_begin + lane; v0 < v_end; v0 += 32 * kUnroll) {
+    // warp-uniform step loop, as in permute_kernel: the shuffles need all
+    // 32 lanes
+    for (int v0 = v_begin; v0 < v_end; v0 += 32 * kUnroll) {
       float acc[kUnroll][N];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u)
@@ -108,7 +114,7 @@ __global__ void __launch_bounds__(kRowWarps * 32)
         uint4 buf[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-          const int v = v0 + u * 32;
+          const int v = v0 + lane + u * 32;
           if (v < v_end) buf[u] = ld_nc_v4(src + v);
         }
 #pragma unroll
@@ -121,7 +127,7 @@ __global__ void __launch_bounds__(kRowWarps * 32)
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int v = v0 + u * 32;
+        const int v = v0 + lane + u * 32;
         if (v < v_end) st_v4(out + v, Vec16<T>::from_f32(acc[u]));
       }
     }

@@ -445,7 +445,14 @@ def test_sigmoid_key_bit_exact():
     # rows cut into 2 segments of 192 vectors, and into 4 with drops
     (777, 2, 8, 3072, torch.bfloat16, 0), (500, 2, 8, 2048, torch.float32, 40),
     # top-1 at capacity, most tokens dropped whole: their rows are not read
-    (4000, 1, 64, 1024, torch.bfloat16, 30)])
+    (4000, 1, 64, 1024, torch.bfloat16, 30),
+    # more tokens than the grid's 148 x 64 warps, so warps take a
+    # second token, with rows of 16 vectors (fewer than a warp's lanes), of
+    # 129 vectors (one past a step of 128) and of 10 vectors; k = 1 and 4
+    # take the general combine loop
+    (12000, 1, 64, 128, torch.bfloat16, 100),
+    (12000, 1, 8, 516, torch.float32, 0),
+    (10000, 4, 16, 40, torch.float32, 1500)])
 def test_permute_combine_parity(T, k, E, D, dt, cap):
     idx = _idx("distinct", T, k, E, seed=D)
     lay = O.dispatch_layout(idx, E, 1, cap if cap > 0 else None)
