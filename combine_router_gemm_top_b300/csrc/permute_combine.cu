@@ -134,19 +134,20 @@ __global__ void __launch_bounds__(kRowWarps * 32)
   }
 }
 
-// k = 2: both slots' row vectors are loaded before any arithmetic, so a
-// step costs one memory round trip instead of two; each vector is then
+// k = KS <= 2: every slot's row vectors are loaded before any arithmetic,
+// so a step costs one memory round trip instead of k; each vector is then
 // reduced and stored on its own, so only its 8 (bf16) accumulators are live
 // and the block fits 4 times per SM.  The fp32 operations and their
-// order are combine_kernel's: y = fma(g1, x1, fma(g0, x0, 0)), a dropped slot
-// skipped.
-template <typename T, bool SEG>
+// order are combine_kernel's: y = fma(g1, x1, fma(g0, x0, 0)) (k = 2) or
+// fma(g0, x0, 0) (k = 1), a dropped slot skipped.
+template <typename T, bool SEG, int KS>
 __global__ void __launch_bounds__(kRowWarps * 32, 4)
     combine2_kernel(int64_t n_tok, int nvec, int nseg_arg,
                     const uint4* __restrict__ yp,
                     const int32_t* __restrict__ dst_row,
                     const float* __restrict__ gate, uint4* __restrict__ y,
                     int max_rows, int32_t* status) {
+  static_assert(KS == 1 || KS == 2, "one or two slots");
   constexpr int N = Vec16<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t warp_g = static_cast<int64_t>(blockIdx.x) * kRowWarps + (threadIdx.x >> 5);
@@ -158,14 +159,15 @@ __global__ void __launch_bounds__(kRowWarps * 32, 4)
     const int v_begin = static_cast<int>(u - t * nseg) * segv;
     const int v_end = v_begin + segv;
     const int32_t my_dst = checked_row(
-        lane < 2 ? __ldg(dst_row + t * 2 + lane) : -1, max_rows, status);
+        lane < KS ? __ldg(dst_row + t * KS + lane) : -1, max_rows, status);
     const float my_g =
-        lane < 2 ? (gate != nullptr ? __ldg(gate + t * 2 + lane) : 1.0f)
-                 : 0.0f;
+        lane < KS ? (gate != nullptr ? __ldg(gate + t * KS + lane) : 1.0f)
+                  : 0.0f;
     const int32_t r0 = __shfl_sync(0xffffffffu, my_dst, 0);
-    const int32_t r1 = __shfl_sync(0xffffffffu, my_dst, 1);
+    // lane 1 holds -1 when k = 1, so the second slot is skipped throughout
+    const int32_t r1 = KS == 2 ? __shfl_sync(0xffffffffu, my_dst, 1) : -1;
     const float g0 = __shfl_sync(0xffffffffu, my_g, 0);
-    const float g1 = __shfl_sync(0xffffffffu, my_g, 1);
+    const float g1 = KS == 2 ? __shfl_sync(0xffffffffu, my_g, 1) : 0.0f;
     const uint4* s0 = yp + static_cast<int64_t>(r0 < 0 ? 0 : r0) * nvec;
     const uint4* s1 = yp + static_cast<int64_t>(r1 < 0 ? 0 : r1) * nvec;
     uint4* out = y + t * nvec;
@@ -253,10 +255,19 @@ moe_status launch_combine(int T, int k, int D, int dtype, const void* yp,
   uint4* dst = static_cast<uint4*>(y);
   if (k == 2 && dtype == MOE_BF16) {
     if (nseg > 1)
-      combine2_kernel<__nv_bfloat16, true><<<grid, kRowWarps * 32, 0, stream>>>(
+      combine2_kernel<__nv_bfloat16, true, 2><<<grid, kRowWarps * 32, 0, stream>>>(
           T, nvec, nseg, src, dst_row, gate, dst, max_rows, status);
     else
-      combine2_kernel<__nv_bfloat16, false><<<grid, kRowWarps * 32, 0, stream>>>(
+      combine2_kernel<__nv_bfloat16, false, 2><<<grid, kRowWarps * 32, 0, stream>>>(
+          T, nvec, 1, src, dst_row, gate, dst, max_rows, status);
+    return launch_status();
+  }
+  if (k == 1 && dtype == MOE_BF16) {
+    if (nseg > 1)
+      combine2_kernel<__nv_bfloat16, true, 1><<<grid, kRowWarps * 32, 0, stream>>>(
+          T, nvec, nseg, src, dst_row, gate, dst, max_rows, status);
+    else
+      combine2_kernel<__nv_bfloat16, false, 1><<<grid, kRowWarps * 32, 0, stream>>>(
           T, nvec, 1, src, dst_row, gate, dst, max_rows, status);
     return launch_status();
   }
